@@ -1,0 +1,201 @@
+/*
+ * libspecverify: the verify-and-commit step of speculative decoding, on one GPU.
+ *
+ * Given the target model's logits for an anchor plus its draft positions, each
+ * call scans every vocabulary row once on the GPU, decides how many drafts are
+ * accepted, produces the correction / bonus token, and emits the KV-commit
+ * index lists for the accepted positions.  Each round yields r + 1 tokens
+ * (r accepted drafts plus one correction or bonus).
+ *
+ * Sources, cited as page title and section:
+ *   [E2D] "从 EAGLE 到 DFlash 2：SGLang 与 SpecForge 的投机解码训练和推理"
+ *         (tom-jerr.github.io/sglang/eagle2-in-sglang)
+ *   [SGO] SGLang speculative-decoding overview (zdszero.github.io/speculative_decoding.html)
+ *
+ * Row convention (row-aligned verify input, [E2D] §1.1 and the verify_ids_2d
+ * construction in §5.6): the target runs on [a, d1 .. dm]; row i of a request
+ * carries input token verify_ids[i] (the anchor a at the request's first row)
+ * and its logits give the distribution that tests verify_ids[i + 1].  The last
+ * row of a request is only used for the bonus token.
+ *
+ * Memory and execution rules shared by every entry point:
+ *   - Every array argument is a DEVICE pointer owned by the caller.  The
+ *     library never allocates, never synchronises the stream and never reads
+ *     device memory from the host; all work is enqueued on `stream`.
+ *   - logits: [rows, ld] row-major, fp32 or bf16 (raw bits), ld >= vocab.  The
+ *     base pointer must be 16-byte aligned and ld * element_size a multiple of
+ *     16.  The same rules hold for q ([rows, ldq] fp32).
+ *   - Host-side argument errors return a status code before anything is
+ *     enqueued.  Data errors found on the device are reported per request in
+ *     out->dev_status (bits below) and still produce defined outputs.
+ *   - ws / ws_bytes: scratch of at least spec_verify_workspace_bytes(...)
+ *     bytes, 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE.  Every call
+ *     whose kernels run to completion leaves the workspace's counter words at
+ *     zero again, so a workspace can be reused by later calls on the same
+ *     stream without clearing.  Calls that share a workspace must not overlap
+ *     on the GPU.
+ *   - Temperature: a request with temperature T samples iff 1e-30 <= T < inf;
+ *     any other value (0, negative, NaN, inf) verifies that request greedily
+ *     ([E2D] §6.5: greedy rows carry a one-hot q).
+ *   - Uniforms are supplied by the caller in [0, 1): u_accept[row] decides the
+ *     acceptance test at that row (for trees: at that node's row), u_final[b]
+ *     draws the request's one correction / bonus token.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_NULL_ARG = 1,            /* a required pointer is NULL                        */
+  SV_ERR_BAD_SHAPE = 2,           /* a size or stride is out of range                  */
+  SV_ERR_BAD_DTYPE = 3,           /* dtype is not SV_F32 or SV_BF16                    */
+  SV_ERR_MISALIGNED = 4,          /* a base pointer or row stride breaks 16-byte rule  */
+  SV_ERR_UNSUPPORTED = 5,         /* a combination the library does not implement     */
+  SV_ERR_WORKSPACE_TOO_SMALL = 6, /* ws is NULL, too small or not 256-byte aligned     */
+  SV_ERR_CUDA = 7                 /* a CUDA launch or device query failed              */
+} sv_status_t;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype_t;
+
+/* Per-request device status bits (out->dev_status[b], OR-ed). */
+#define SV_DEV_TOKEN_RANGE 1u    /* a tested draft / child token is outside [0, vocab): it is rejected   */
+#define SV_DEV_NONFINITE 2u      /* a visited row had NaN / +inf entries (ignored) or was all -inf;      */
+                                 /* an all -inf row stops verification there and its token is -1          */
+#define SV_DEV_BAD_TREE 4u       /* parents / sibling lists invalid: the request is verified as its root  */
+#define SV_DEV_BAD_LAYOUT 8u     /* cu_seqlens range invalid: nothing committed, num_out 0, bonus -1      */
+#define SV_DEV_RESIDUAL_EMPTY 16u /* residual mass was <= 0: the token was sampled from p instead         */
+#define SV_DEV_DUP_SIBLING 32u   /* target-only tree: a sibling repeats a token; the repeat is skipped    */
+
+/*
+ * Outputs of one call (all DEVICE pointers, caller-owned).  max_len is the
+ * per-request row bound of the call (chains: m + 1; ragged: max_len; trees:
+ * nodes).  [E2D] §5.6.6 and §8.1 table; [SGO] "两个容易误解的工程细节".
+ */
+typedef struct {
+  int32_t* accept_len;      /* [B] r, accepted drafts                                        */
+  int32_t* num_out;         /* [B] r + 1 (= commit_lens); 0 for a bad layout                  */
+  int32_t* out_tokens;      /* [B, max_len] accepted drafts then the bonus; rest -1           */
+  int32_t* bonus;           /* [B] correction / bonus token (-1 when no usable row)          */
+  int32_t* accept_rows;     /* [B, max_len] global logits rows committed: anchor row, then    */
+                            /*   the rows of the accepted drafts / tree path; rest -1          */
+  int32_t* commit_cu;       /* [B + 1] exclusive scan of num_out                              */
+  int64_t* commit_src_slot; /* [rows] or NULL: row_slots[accept_rows[b][k]] at commit_cu[b]+k */
+  int64_t* commit_dst_pos;  /* [rows] or NULL: seq_lens[b] + k at commit_cu[b] + k            */
+  uint32_t* dev_status;     /* [B] SV_DEV_* bits                                              */
+} sv_out_t;
+
+/* Bytes of workspace needed for a call with these sizes (rows = total logits
+ * rows, max_len = per-request row bound / tree nodes). */
+size_t spec_verify_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len);
+
+/* Static description of a status code. */
+const char* spec_verify_status_string(sv_status_t status);
+
+/*
+ * Greedy chain verification ([E2D] §1.2 first bullet; [SGO] "为什么结果不受
+ * draft 影响": accept while the target argmax equals the draft, else replace
+ * it with the argmax and stop).  batch requests of m drafts each: rows =
+ * batch * (m + 1), request b owns rows [b*(m+1), (b+1)*(m+1)).  Argmax ties
+ * resolve to the lowest index.  row_slots [rows] and seq_lens [B] (int64) are
+ * only needed for commit_src_slot / commit_dst_pos.
+ */
+sv_status_t spec_verify_greedy_chain(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch, int32_t m,
+                                     int32_t vocab, const int32_t* verify_ids, const int64_t* row_slots,
+                                     const int64_t* seq_lens, const sv_out_t* out, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/*
+ * Greedy tree verification ([SGO] "为什么结果不受 draft 影响", verify_tree_greedy;
+ * [E2D] §2.4, §3.4).  Request b has `nodes` nodes (node 0 = root / anchor);
+ * node i owns logits row b*nodes + i, carries token tokens[b][i] and has parent
+ * parents[b][i] (-1 for the root, otherwise 0 <= parent < i).  From the root,
+ * the walk moves to the first child (ascending node index, or the order of the
+ * optional first_child / next_sibling lists, both [B, nodes], -1 terminated)
+ * whose token equals the current row's argmax; the bonus is the argmax of the
+ * last node's row.  nodes <= 1024.
+ */
+sv_status_t spec_verify_greedy_tree(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch, int32_t nodes,
+                                    int32_t vocab, const int32_t* tokens, const int32_t* parents,
+                                    const int32_t* first_child, const int32_t* next_sibling,
+                                    const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * p/q rejection chain ([E2D] §1.2: alpha = min(1, p/q), residual
+ * p' = [p - q]_+ / sum [p - q]_+; temperature-scaled softmax p = softmax(l/T),
+ * §6.2).  Row j of a request accepts its draft d iff u_accept[row] * q[row][d]
+ * < p_row(d); at the first rejection the correction is drawn from the residual
+ * of that row, and when every draft passes the bonus is drawn from p of the
+ * last row.  Draws use inverse CDF: the smallest v whose running weight sum
+ * exceeds u_final[b] * S (§6.2, sample_path()).  q [rows, ldq] fp32 is the
+ * proposal actually sampled from ([E2D] §5.6.1, §6.5); the last row of each
+ * request is never read.  temperature [B], u_accept [rows], u_final [B] fp32.
+ */
+sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch, int32_t m,
+                                        int32_t vocab, const int32_t* verify_ids, const float* q, int64_t ldq,
+                                        const float* temperature, const float* u_accept, const float* u_final,
+                                        const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
+                                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Ragged p/q rejection ([E2D] §5.6.5: verify_lens include the anchor, compact
+ * offsets, e.g. lens [4,2,6] -> [0,4,6,12]).  Request b owns rows
+ * [cu_seqlens[b], cu_seqlens[b+1]) of the total_rows rows; lengths must lie in
+ * [1, max_len] (length 1 = bonus only).  A request whose range is invalid gets
+ * SV_DEV_BAD_LAYOUT and commits nothing.  Otherwise as the rejection chain.
+ */
+sv_status_t spec_verify_rejection_ragged(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                         int64_t total_rows, int32_t max_len, int32_t vocab,
+                                         const int32_t* cu_seqlens, const int32_t* verify_ids, const float* q,
+                                         int64_t ldq, const float* temperature, const float* u_accept,
+                                         const float* u_final, const int64_t* row_slots, const int64_t* seq_lens,
+                                         const sv_out_t* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Target-only tree sampling ([SGO] "为什么结果不受 draft 影响":
+ * tree_speculative_sampling_target_only uses only target probabilities, draft
+ * probabilities passed as 0, thresholds default 1.0).  At node cur with
+ * uniform u = u_accept[row(cur)], children are visited in order with
+ * c += p_cur(token); the first child with u < c / threshold_acc or
+ * p_cur(token) >= threshold_single is accepted.  A sibling repeating an
+ * earlier sibling's token is skipped (SV_DEV_DUP_SIBLING).  If no child is
+ * accepted the final token is drawn from p_cur with the children's tokens
+ * zeroed; at a leaf, from p_leaf.  With both thresholds 1.0 the output law
+ * equals the target's.  threshold_acc must be > 0 and finite.  Tree layout as
+ * in spec_verify_greedy_tree.
+ */
+sv_status_t spec_verify_target_only_tree(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                         int32_t nodes, int32_t vocab, const int32_t* tokens,
+                                         const int32_t* parents, const int32_t* first_child,
+                                         const int32_t* next_sibling, const float* temperature,
+                                         float threshold_single, float threshold_acc, const float* u_accept,
+                                         const float* u_final, const int64_t* row_slots, const int64_t* seq_lens,
+                                         const sv_out_t* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Row statistics on their own (the single pass every entry point starts
+ * with): for each of `rows` rows, the maximum M (float), the lowest argmax
+ * (-1 for an all -inf row), Z = sum_v exp((l_v - M)/T) with T = row_temp[row]
+ * (0 when row_temp is NULL or the row is greedy), p at probe[row] (when
+ * probe and out_p are given), and SV_DEV_NONFINITE in row_flags.
+ * out_z is double.  All outputs [rows]; out_p / probe / row_temp may be NULL.
+ */
+sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t ld, int64_t rows, int32_t vocab,
+                                  const float* row_temp, const int32_t* probe, float* out_max,
+                                  int32_t* out_argmax, double* out_z, float* out_p, uint32_t* row_flags,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -33,7 +33,8 @@
 //   * residual mass S <= 0: sample from p instead and set status bit 16.
 //   * argmax ties: lowest index.  NaN and +inf elements are excluded (status bit 2); a row
 //     with no finite-or-(-inf) maximum (all -inf) is unusable: stop there, bonus -1.
-//   * temperature <= 0 (or NaN) for a request: that request is verified greedily.
+//   * a request samples iff 1e-30 <= T < inf ([E2D] §6.2: T > 0 rows sample, greedy rows take
+//     the argmax); any other temperature (0, negative, NaN, inf, tiny) is verified greedily.
 //   * target-only tree: at node cur with uniform u, walk the children in order, c += p(tok);
 //     accept the first child with u < c/theta_acc or p(tok) >= theta_single.  A child whose
 //     token repeats an earlier sibling's is skipped (status bit 32).  If none is accepted,
@@ -98,6 +99,8 @@ struct RowDist {
 
 bool usable(double l) { return !std::isnan(l) && l != kInf; }
 
+bool sampling_temperature(double T) { return T >= 1e-30 && T < kInf; }
+
 RowDist row_dist(const Logits& lg, int64_t row, double T) {
   RowDist r;
   r.T = T;
@@ -112,7 +115,7 @@ RowDist row_dist(const Logits& lg, int64_t row, double T) {
       r.argmax = v;
     }
   }
-  if (T > 0.0 && r.argmax >= 0) {
+  if (T > 0.0 && r.argmax >= 0) {  // callers pass T = 0 for greedy rows
     double Z = 0.0;
     for (int64_t v = 0; v < lg.vocab; ++v) {
       double l = lg.at(row, v);
@@ -266,8 +269,9 @@ ReqResult verify_chain_request(const ChainArgs& a, int32_t b) {
     rr.gap = kInf;
     return rr;
   }
-  const double T = a.greedy_all ? 0.0 : static_cast<double>(a.temperature[b]);
-  const bool greedy = !(T > 0.0);
+  const double Tb = a.greedy_all ? 0.0 : static_cast<double>(a.temperature[b]);
+  const bool greedy = !sampling_temperature(Tb);
+  const double T = greedy ? 0.0 : Tb;
   rr.rows.push_back(static_cast<int32_t>(start));
 
   enum { kAllAccepted, kRejected, kUnusable } how = kAllAccepted;
@@ -396,8 +400,9 @@ ReqResult verify_tree_request(const TreeArgs& a, int32_t b) {
   const int32_t* tok = a.tokens + row0;
   const bool ok_tree = tree_valid(a, b);
   if (!ok_tree) rr.status |= kBadTree;
-  const double T = (a.mode == 1) ? static_cast<double>(a.temperature[b]) : 0.0;
-  const bool greedy = !(T > 0.0);
+  const double Tb = (a.mode == 1) ? static_cast<double>(a.temperature[b]) : 0.0;
+  const bool greedy = !sampling_temperature(Tb);
+  const double T = greedy ? 0.0 : Tb;
 
   int32_t cur = 0;
   rr.rows.push_back(static_cast<int32_t>(row0));
@@ -546,6 +551,7 @@ int oracle_row_stats(const void* logits, int dtype, int64_t ld, int64_t rows, in
   Logits lg{logits, dtype, ld, vocab};
   for (int64_t r = 0; r < rows; ++r) {
     double T = row_temp ? static_cast<double>(row_temp[r]) : 0.0;
+    if (!sampling_temperature(T)) T = 0.0;
     RowDist st = row_dist(lg, r, T);
     out_max[r] = st.M;
     out_argmax[r] = static_cast<int32_t>(st.argmax);
@@ -565,8 +571,9 @@ int oracle_row_stats(const void* logits, int dtype, int64_t ld, int64_t rows, in
 int oracle_row_probs(const void* logits, int dtype, int64_t ld, int64_t row, int32_t vocab, double T,
                      double* p_out) {
   Logits lg{logits, dtype, ld, vocab};
+  if (!sampling_temperature(T)) return -1;
   RowDist st = row_dist(lg, row, T);
-  if (st.argmax < 0 || !(T > 0.0)) return -1;
+  if (st.argmax < 0) return -1;
   std::vector<double> p;
   row_probs(lg, row, st, p);
   std::copy(p.begin(), p.end(), p_out);
