@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verify-and-commit step on one GB300.
+
+One step is one call of the entry point the workload names: row statistics
+over every logits row, acceptance, the correction / bonus draw and the KV
+commit for the whole batch, on inputs already resident in HBM.  The default
+workload is the DFlash-style block (64 requests x 16 rows, V = 151936, bf16
+logits, full p/q rejection with residual sampling and bonus).
+
+Prints one JSON line on rank 0.  `--impl reference` times the fp64 CPU oracle
+on the host cores instead (the only reference this path has).
+Multi-GPU (torchrun): every rank verifies its own batch (weak scaling, no
+collective on the data path); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s"
+UNIT = "rows/s"
+KERNELS_PER_STEP = {"greedy_chain": 3, "greedy_tree": 3, "rejection_chain": 4, "rejection_ragged": 4,
+                    "target_only_tree": 4}
+STATS_SOURCES = ("reject_row_vocab_gb300/csrc/sv_stats.cu", "reject_row_vocab_gb300/csrc/sv_device.cuh")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--tree-mode", default="target_only_tree", choices=["greedy_tree", "target_only_tree"])
+    ap.add_argument("--eager", action="store_true", help="launch every step from Python instead of a CUDA graph")
+    ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Ranks
+# ---------------------------------------------------------------------------
+
+
+class Ranks:
+    """torchrun environment; every data-path step stays local to its rank."""
+
+    def __init__(self, backend: str | None = None):
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        self.backend = backend
+        if self.world > 1:
+            import torch.distributed as dist
+            if backend is None:
+                import torch
+                backend = "nccl" if torch.cuda.is_available() else "gloo"
+            self.backend = backend
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if self.pg is None:
+            return float(x)
+        import torch
+        dev = "cuda" if self.backend == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def rank_seed(index: int, rank: int) -> int:
+    """Rank r verifies its own batch: the named workload's seed, shifted per rank."""
+    return 1000 + index + 100 * rank
+
+
+def whole_job_value(units_per_rank: list, max_seconds: float) -> float:
+    return float(sum(units_per_rank)) / max_seconds
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+
+
+class ClockSampler:
+    FIELDS = ("timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "25", "-i", self.gpu_id], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not runnable"}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts + frac, float(parts[1]), float(parts[2]), parts[3], parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        use = inside if inside else rows
+        if not use:
+            return {"unavailable": "no samples"}
+        reasons = sorted({n for r in use for n, v in zip(self.NAMES, r[4]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "in_window": bool(inside)}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device_index)
+
+
+# ---------------------------------------------------------------------------
+# Shared pieces
+# ---------------------------------------------------------------------------
+
+
+def measured_peaks() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def stats_traffic() -> float | None:
+    """dram bytes per row-statistics launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for p in STATS_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    if rec.get("source_sha256") != h.hexdigest():
+        return None
+    return rec.get("bytes_per_full_launch")
+
+
+def make_workload(args, rank: int = 0):
+    from reject_row_vocab_gb300 import workload as wl
+    kw = {"seed": rank_seed(args.config, rank)}
+    if args.config == 3:
+        kw["mode"] = args.tree_mode
+    return wl.config(args.config, **kw)
+
+
+def describe(w) -> dict:
+    return {"workload": w.name, "kind": w.kind, "batch": w.batch, "rows": w.rows, "vocab": w.vocab,
+            "max_len": w.max_len, "logit_dtype": w.dtype, "logit_bytes": w.logit_bytes(),
+            "l2": "inputs larger than L2 (%.0f MB of logits vs 129 MB L2)" % (w.logit_bytes() / 1e6)
+            if w.logit_bytes() > 129e6 else "inputs smaller than L2: repeated steps may hit in L2",
+            "seed": w.meta.get("seed")}
+
+
+def oracle_run(w, threads: int):
+    import oracle
+    if w.kind == "greedy_chain":
+        return oracle.verify_chain(w, greedy_all=True, threads=threads)
+    if w.kind in ("rejection_chain", "rejection_ragged"):
+        return oracle.verify_chain(w, threads=threads)
+    return oracle.verify_tree(w, "greedy" if w.kind == "greedy_tree" else "target_only", threads=threads)
+
+
+def time_oracle(w, seconds: float, threads: int) -> dict:
+    """The oracle, as it stands, on the host cores over the full batch, repeated for ~`seconds`."""
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_run(w, threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": w.rows * reps / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "full batch (%d requests, %d rows) x %d repetitions, std::thread over requests"
+                      % (w.batch, w.rows, reps), "seconds": round(el, 3)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args):
+    import torch
+    ranks = Ranks()
+    torch.cuda.set_device(ranks.local)
+    from reject_row_vocab_gb300 import _build
+    if ranks.local == 0:
+        _build.build()
+    ranks.barrier()
+    from reject_row_vocab_gb300 import device_workload as dw
+    from reject_row_vocab_gb300 import specverify as sv
+
+    w = make_workload(args, ranks.rank)
+    d = dw.DeviceInputs.from_workload(w)
+    out = dw.outputs_for(w)
+    ws = dw.workspace_for(w)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+
+    for _ in range(max(W, 3)):
+        dw.run(w, d, out=out, ws=ws)
+    torch.cuda.synchronize()
+
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    G = max(1, min(args.graph_steps, K))
+    P = min(K, 1024) if args.eager else G  # event pairs around the row-statistics kernel
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(P)]
+    for a, b in pairs:  # create the events on the device
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            dw.run(w, d, out=out, ws=ws)  # populate per-device caches outside capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for k in range(G):
+                sv.set_stats_events(*pairs[k])
+                dw.run(w, d, out=out, ws=ws)
+            sv.set_stats_events(None, None)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(gpu_id_for(ranks.local))
+    clocks.start()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev_start.record(stream)
+    if graph is None:
+        for k in range(K):
+            sv.set_stats_events(*pairs[k % P])
+            dw.run(w, d, out=out, ws=ws)
+        sv.set_stats_events(None, None)
+        launched = K
+    else:
+        reps = max(1, K // G)
+        for _ in range(reps):
+            graph.replay()
+        launched = reps * G
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    t1 = time.time()
+    clocks.mark(t0, t1)
+    clk = clocks.stop()
+
+    elapsed_s = ev_start.elapsed_time(ev_end) / 1e3
+    max_s = ranks.max(elapsed_s)
+    avg_stats_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)  # last recording of each pair
+
+    res = out.to_numpy()
+    committed = int(res["num_out"].sum())
+    rows_total = ranks.sum(w.rows * launched)
+    value = rows_total / max_s
+    tokens = ranks.sum(committed * launched) / max_s
+    peak, peak_src = measured_peaks()
+    alg_bytes = w.logit_bytes()
+    achieved = alg_bytes / (avg_stats_ms / 1e3) / 1e9
+
+    # end to end through the public call with host buffers: H2D inputs, verify, D2H results
+    e2e = None
+    if args.e2e_steps > 0:
+        host = dw.DeviceInputs.from_workload(w, pin=True)
+        out_names = ("accept_len", "num_out", "out_tokens", "bonus", "commit_cu", "commit_src_slot",
+                     "commit_dst_pos", "dev_status")
+        h_out = {n: torch.empty_like(getattr(out, n), device="cpu").pin_memory() for n in out_names}
+        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        h2d = host.nbytes()
+        for _ in range(2):
+            d.copy_from(host)
+            dw.run(w, d, out=out, ws=ws)
+        torch.cuda.synchronize()
+        ranks.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            d.copy_from(host)
+            dw.run(w, d, out=out, ws=ws)
+            for n in out_names:
+                h_out[n].copy_(getattr(out, n), non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_s = ranks.max(e0.elapsed_time(e1) / 1e3)
+        e2e = {"value": ranks.sum(w.rows * args.e2e_steps) / e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e_s / args.e2e_steps}
+
+    cpu = None
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle(w, args.cpu_seconds, os.cpu_count() or 1)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": launched,
+        "warmup": max(W, 3), "ms_per_step": 1e3 * max_s / launched, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": dict(describe(w), launch="eager" if graph is None else "cuda graph of %d steps" % G,
+                       parallelism="replicas x%d (independent batches)" % ranks.world),
+        "committed_tokens_per_s": tokens, "mean_accept_len": float(res["accept_len"].mean()),
+        "logit_gbs_per_step": alg_bytes * launched / elapsed_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": stats_traffic(), "kernel": "k_row_stats", "bytes_per_launch": alg_bytes,
+                     "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
+        "clocks": clk, "gpu_launches": KERNELS_PER_STEP[w.kind] * launched,
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+    ranks.close()
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = make_workload(args, 0)
+    threads = os.cpu_count() or 1
+    K, W = args.steps, max(args.warmup, 3)
+    t0 = time.perf_counter()
+    oracle_run(w, threads)
+    per_batch = time.perf_counter() - t0
+    # each step verifies the full batch when the budget allows, else a prefix of its requests
+    budget = args.ref_budget_s / (K + W)
+    n = w.batch if per_batch <= budget else max(1, int(w.batch * budget / per_batch))
+    sub = subset(w, n)
+    for _ in range(W):
+        oracle_run(sub, threads)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_run(sub, threads)
+    el = time.perf_counter() - t0
+    value = sub.rows * K / el
+    sample = "%d of %d requests (%d rows) per step, %d steps, std::thread over requests" % (n, w.batch, sub.rows, K)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": 1e3 * el / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": dict(describe(w), parallelism="host cores"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def subset(w, n: int):
+    """The first n requests of a workload (slicing only)."""
+    import copy
+    if n >= w.batch:
+        return w
+    s = copy.copy(w)
+    if w.nodes:
+        rows = n * w.nodes
+        s.tokens, s.parents = w.tokens[:n], w.parents[:n]
+        if w.first_child is not None:
+            s.first_child, s.next_sibling = w.first_child[:n], w.next_sibling[:n]
+    else:
+        rows = int(w.cu_seqlens[n])
+        s.cu_seqlens = w.cu_seqlens[: n + 1]
+        s.verify_ids = w.verify_ids[:rows]
+    s.batch, s.rows = n, rows
+    s.logits = w.logits[:rows]
+    for k in ("q", "u_accept", "row_slots"):
+        if getattr(w, k) is not None:
+            setattr(s, k, getattr(w, k)[:rows])
+    for k in ("temperature", "u_final", "seq_lens"):
+        if getattr(w, k) is not None:
+            setattr(s, k, getattr(w, k)[:n])
+    return s
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

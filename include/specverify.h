@@ -56,7 +56,7 @@ extern "C" {
 typedef enum {
   SV_OK = 0,
   SV_ERR_NULL_ARG = 1,            /* a required pointer is NULL                        */
-  SV_ERR_BAD_SHAPE = 2,           /* a size or stride is out of range                  */
+  SV_ERR_BAD_SHAPE = 2,           /* a size, stride or scalar argument is out of range */
   SV_ERR_BAD_DTYPE = 3,           /* dtype is not SV_F32 or SV_BF16                    */
   SV_ERR_MISALIGNED = 4,          /* a base pointer or row stride breaks 16-byte rule  */
   SV_ERR_UNSUPPORTED = 5,         /* a combination the library does not implement     */
@@ -99,6 +99,14 @@ size_t spec_verify_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, i
 
 /* Static description of a status code. */
 const char* spec_verify_status_string(sv_status_t status);
+
+/* Benchmark instrumentation (not needed for verification).  While set, every
+ * call made from this host thread records `start` on its stream immediately
+ * before its row-statistics kernel and `stop` immediately after it, so the
+ * caller can time that kernel with cudaEventElapsedTime.  The events are the
+ * caller's; pass NULL, NULL to stop.  Returns SV_ERR_NULL_ARG if exactly one
+ * of the two is NULL. */
+sv_status_t spec_verify_set_stats_events(cudaEvent_t start, cudaEvent_t stop);
 
 /*
  * Greedy chain verification ([E2D] §1.2 first bullet; [SGO] "为什么结果不受

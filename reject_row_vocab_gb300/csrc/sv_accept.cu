@@ -1,0 +1,323 @@
+// Acceptance: one warp per request decides how many drafts are accepted.
+//
+// Chains and ragged blocks ([E2D] §1.1, §1.2, §5.6.5): every lane takes one
+// verify row, evaluates its test (greedy: argmax == draft; sampling:
+// u * q(d) < p(d) with p = 2^((l_d - M) k) / Z, [E2D] §1.2 equation for
+// alpha), and a warp ballot finds the first failure.  Trees ([SGO]
+// "为什么结果不受 draft 影响": verify_tree_greedy and
+// tree_speculative_sampling_target_only): the walk goes from the root, the
+// children of the current node are found with a ballot over the parent
+// array, and the accepted child is the first (ballot) match.
+//
+//   [E2D] "从 EAGLE 到 DFlash 2：SGLang 与 SpecForge 的投机解码训练和推理"
+//   [SGO] SGLang speculative-decoding overview (zdszero.github.io)
+//
+// Each request leaves in the workspace what the final-token step must do
+// (nothing, residual draw, bonus draw, or bonus draw with excluded tokens),
+// and writes its accepted prefix straight into the outputs.
+#include <cstdint>
+
+#include "sv_device.cuh"
+#include "sv_internal.h"
+
+namespace sv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kChainWarps = 4;
+
+__device__ __forceinline__ uint32_t warp_or(uint32_t v) { return __reduce_or_sync(kFull, v); }
+
+// p_row(token) from the row statistics; 0 for an excluded (NaN / +inf) entry.
+__device__ __forceinline__ double target_prob(const LogitsView& lg, int64_t row, int32_t tok, const RowStat& rs) {
+  const float l = load_logit(lg, row, tok);
+  if (!usable_logit(l)) return 0.0;
+  return static_cast<double>(exp2f((l - rs.M) * rs.k)) / rs.Z;
+}
+
+__global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kChainWarps + (threadIdx.x >> 5);
+  if (b >= p.batch) return;
+  const int ML = p.max_len;
+  int32_t* otok = out.out_tokens + static_cast<int64_t>(b) * ML;
+  int32_t* orow = out.accept_rows + static_cast<int64_t>(b) * ML;
+
+  int64_t start, end;
+  if (p.fixed_len > 0) {
+    start = static_cast<int64_t>(b) * p.fixed_len;
+    end = start + p.fixed_len;
+  } else {
+    start = p.cu[b];
+    end = p.cu[b + 1];
+  }
+  const int64_t L = end - start;
+  if (start < 0 || end > p.lg.rows || L < 1 || L > ML) {  // invalid layout: commit nothing
+    for (int k = lane; k < ML; k += 32) {
+      otok[k] = -1;
+      orow[k] = -1;
+    }
+    if (lane == 0) {
+      out.accept_len[b] = 0;
+      out.num_out[b] = 0;
+      out.bonus[b] = -1;
+      out.dev_status[b] = kStBadLayout;
+      ws.state[b] = ReqState{0, -1, kModeNoCommit, -1, kStBadLayout, 0, 0, 0};
+    }
+    return;
+  }
+
+  const float T = p.temperature ? p.temperature[b] : 0.0f;
+  const bool greedy = !sampling_temperature(T);
+  uint32_t st = 0u;
+  int64_t s = L - 1;  // row (within the request) that yields the final token
+  int how = 0;        // 0 all accepted, 1 rejected, 2 unusable row
+  for (int64_t j0 = 0; j0 < L - 1; j0 += 32) {
+    const int64_t j = j0 + lane;
+    const bool active = j < L - 1;
+    int stop = 0;
+    uint32_t fl = 0u;
+    if (active) {
+      const int64_t row = start + j;
+      const RowStat rs = ws.rowstat[row];
+      fl = rs.flags;
+      if (rs.argmax < 0) {
+        stop = 2;
+        fl |= kStNonFinite;
+      } else {
+        const int32_t d = p.ids[row + 1];
+        if (d < 0 || d >= p.lg.vocab) {
+          stop = 1;
+          fl |= kStTokenRange;
+        } else if (greedy) {
+          stop = (rs.argmax != d) ? 1 : 0;
+        } else {
+          const double pd = target_prob(p.lg, row, d, rs);
+          const double qd = static_cast<double>(p.q[row * p.ldq + d]);
+          const double u = static_cast<double>(p.u_accept[row]);
+          stop = (u * qd < pd) ? 0 : 1;
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(kFull, active && stop != 0);
+    const int first = bal ? __ffs(bal) - 1 : 32;
+    st |= warp_or((active && lane <= first) ? fl : 0u);  // rows past the stop are not visited
+    if (bal) {
+      s = j0 + first;
+      how = __shfl_sync(kFull, stop, first);
+      break;
+    }
+  }
+
+  const int64_t fr = start + s;
+  const RowStat fs = ws.rowstat[fr];
+  st |= fs.flags;
+  int32_t bonus = -1;
+  int32_t mode = kModeDone;
+  if (how == 2 || fs.argmax < 0) {
+    st |= kStNonFinite;
+  } else if (greedy) {
+    bonus = fs.argmax;
+  } else {
+    mode = (how == 1) ? kModeResidual : kModeP;
+  }
+  for (int64_t k = lane; k < ML; k += 32) {
+    int32_t t = -1, r = -1;
+    if (k < s) {
+      t = p.ids[start + 1 + k];
+      r = static_cast<int32_t>(start + k);
+    } else if (k == s) {
+      t = bonus;
+      r = static_cast<int32_t>(start + k);
+    }
+    otok[k] = t;
+    orow[k] = r;
+  }
+  if (lane == 0) {
+    out.accept_len[b] = static_cast<int32_t>(s);
+    out.num_out[b] = static_cast<int32_t>(s + 1);
+    out.bonus[b] = bonus;
+    out.dev_status[b] = st;
+    ws.state[b] = ReqState{static_cast<int32_t>(s), static_cast<int32_t>(fr), mode, bonus, st, 0, 0, 0};
+  }
+}
+
+// One warp per request.  Node data is staged in shared memory.
+__global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, Ws ws) {
+  __shared__ int32_t s_tok[kMaxNodes];
+  __shared__ int32_t s_par[kMaxNodes];
+  __shared__ int32_t s_kid[kMaxNodes];
+  __shared__ double s_pk[kMaxNodes];
+  const int lane = threadIdx.x;
+  const int b = blockIdx.x;
+  const int N = p.nodes;
+  const int V = p.lg.vocab;
+  const int64_t row0 = static_cast<int64_t>(b) * N;
+  int32_t* otok = out.out_tokens + row0;
+  int32_t* orow = out.accept_rows + row0;
+  const bool lists = p.first_child != nullptr;
+  const int32_t* fc = lists ? p.first_child + row0 : nullptr;
+  const int32_t* ns = lists ? p.next_sibling + row0 : nullptr;
+
+  for (int i = lane; i < N; i += 32) {
+    s_tok[i] = p.tokens[row0 + i];
+    s_par[i] = p.parents[row0 + i];
+  }
+  __syncwarp();
+
+  // Validation: parents point strictly backwards, sibling lists (when given)
+  // only list children of their node and end within N steps.
+  bool bad = false;
+  for (int i = lane; i < N; i += 32) {
+    const int32_t pi = s_par[i];
+    if (i == 0 ? pi != -1 : (pi < 0 || pi >= i)) bad = true;
+  }
+  if (lists) {
+    for (int i = lane; i < N; i += 32) {
+      int32_t c = fc[i];
+      for (int steps = 0; c != -1 && !bad; ++steps) {
+        if (steps >= N || c < 1 || c >= N || s_par[c] != i) {
+          bad = true;
+        } else {
+          c = ns[c];
+        }
+      }
+    }
+  }
+  bad = __any_sync(kFull, bad);
+
+  const float T = p.temperature ? p.temperature[b] : 0.0f;
+  const bool greedy = !sampling_temperature(T);
+  uint32_t st = bad ? kStBadTree : 0u;
+  int cur = 0, depth = 0;
+  int32_t bonus = -1;
+  int32_t mode = kModeDone;
+  int32_t n_excl = 0;
+  int64_t sample_row = -1;
+  if (lane == 0) orow[0] = static_cast<int32_t>(row0);
+
+  for (;;) {
+    const int64_t row = row0 + cur;
+    const RowStat rs = ws.rowstat[row];
+    st |= rs.flags;
+    if (rs.argmax < 0) {
+      st |= kStNonFinite;
+      break;
+    }
+    // Children of cur, in verification order, into s_kid[0, nk).
+    int nk = 0;
+    if (!bad) {
+      if (!lists) {
+        for (int i0 = cur + 1; i0 < N; i0 += 32) {
+          const int i = i0 + lane;
+          const bool is_child = i < N && s_par[i] == cur;
+          const unsigned bal = __ballot_sync(kFull, is_child);
+          if (is_child) s_kid[nk + __popc(bal & ((1u << lane) - 1u))] = i;
+          nk += __popc(bal);
+        }
+      } else {
+        if (lane == 0) {
+          for (int32_t c = fc[cur]; c != -1; c = ns[c]) s_kid[nk++] = c;
+        }
+        nk = __shfl_sync(kFull, nk, 0);
+      }
+    }
+    __syncwarp();
+
+    int next = -1;
+    if (greedy) {
+      for (int k0 = 0; k0 < nk; k0 += 32) {
+        const int kk = k0 + lane;
+        const bool valid = kk < nk;
+        const int32_t t = valid ? s_tok[s_kid[kk]] : -1;
+        const bool oor = valid && (t < 0 || t >= V);
+        const bool match = valid && !oor && t == rs.argmax;
+        const unsigned bal = __ballot_sync(kFull, match);
+        const int first = bal ? __ffs(bal) - 1 : 32;
+        if (__any_sync(kFull, oor && lane <= first)) st |= kStTokenRange;
+        if (bal) {
+          next = s_kid[k0 + first];
+          break;
+        }
+      }
+      if (next < 0) {
+        bonus = rs.argmax;
+        break;
+      }
+    } else {
+      for (int kk = lane; kk < nk; kk += 32) {
+        const int32_t t = s_tok[s_kid[kk]];
+        s_pk[kk] = (t >= 0 && t < V) ? target_prob(p.lg, row, t, rs) : 0.0;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const double u = static_cast<double>(p.u_accept[row]);
+        const double th_acc = static_cast<double>(p.th_acc), th_single = static_cast<double>(p.th_single);
+        double c = 0.0;
+        int32_t* excl = ws.excl + static_cast<int64_t>(b) * N;
+        for (int kk = 0; kk < nk; ++kk) {
+          const int32_t t = s_tok[s_kid[kk]];
+          if (t < 0 || t >= V) {
+            st |= kStTokenRange;
+            continue;
+          }
+          bool dup = false;
+          for (int e = 0; e < n_excl; ++e) dup |= (excl[e] == t);
+          if (dup) {
+            st |= kStDupSibling;
+            continue;
+          }
+          excl[n_excl++] = t;
+          const double pk = s_pk[kk];
+          c += pk;
+          if (u < c / th_acc || pk >= th_single) {
+            next = s_kid[kk];
+            break;
+          }
+        }
+      }
+      next = __shfl_sync(kFull, next, 0);
+      n_excl = __shfl_sync(kFull, n_excl, 0);
+      st = __shfl_sync(kFull, st, 0);
+      if (next < 0) {
+        mode = kModePExcl;
+        sample_row = row;
+        break;
+      }
+      n_excl = 0;
+    }
+    ++depth;
+    if (lane == 0) {
+      orow[depth] = static_cast<int32_t>(row0 + next);
+      otok[depth - 1] = s_tok[next];
+    }
+    cur = next;
+  }
+  __syncwarp();
+  for (int k = depth + lane; k < N; k += 32) {
+    otok[k] = (k == depth) ? bonus : -1;
+    if (k > depth) orow[k] = -1;
+  }
+  if (lane == 0) {
+    out.accept_len[b] = depth;
+    out.num_out[b] = depth + 1;
+    out.bonus[b] = bonus;
+    out.dev_status[b] = st;
+    ws.state[b] = ReqState{depth, static_cast<int32_t>(sample_row), mode, bonus, st, n_excl, 0, 0};
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_accept_chain(const ChainParams& p, const OutView& out, const Ws& ws, cudaStream_t stream) {
+  const int blocks = (p.batch + kChainWarps - 1) / kChainWarps;
+  k_accept_chain<<<blocks, 32 * kChainWarps, 0, stream>>>(p, out, ws);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws& ws, cudaStream_t stream) {
+  k_accept_tree<<<p.batch, 32, 0, stream>>>(p, out, ws);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

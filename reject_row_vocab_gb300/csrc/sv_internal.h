@@ -1,0 +1,221 @@
+// Internal layout shared by the CUDA translation units of libspecverify.
+//
+// Not installed, not part of the C ABI: the public interface is
+// include/specverify.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "specverify.h"
+
+namespace sv {
+
+// Per-request status bits (same values as SV_DEV_* in the public header).
+constexpr uint32_t kStTokenRange = SV_DEV_TOKEN_RANGE;
+constexpr uint32_t kStNonFinite = SV_DEV_NONFINITE;
+constexpr uint32_t kStBadTree = SV_DEV_BAD_TREE;
+constexpr uint32_t kStBadLayout = SV_DEV_BAD_LAYOUT;
+constexpr uint32_t kStResidualEmpty = SV_DEV_RESIDUAL_EMPTY;
+constexpr uint32_t kStDupSibling = SV_DEV_DUP_SIBLING;
+
+// Final statistics of one logits row, written by the row-statistics kernel.
+// M is the row maximum over usable entries (finite or -inf), argmax its lowest
+// index (-1 for an all -inf row), k = log2(e)/T (0 for a greedy row) and
+// Z = sum_v 2^((l_v - M) * k) (0 for a greedy row).
+struct RowStat {
+  double Z;
+  float M;
+  int32_t argmax;
+  uint32_t flags;
+  float k;
+};
+static_assert(sizeof(RowStat) == 24, "RowStat layout");
+
+// A CTA's partial statistics for the part of one row it scanned.
+struct RowPartial {
+  double s;  // sum of 2^((l - m) * k) over the part
+  float m;
+  int32_t idx;
+  uint32_t flags;
+  uint32_t pad;
+};
+static_assert(sizeof(RowPartial) == 24, "RowPartial layout");
+
+// What the final-token step has to do for a request.
+enum SampleMode : int32_t {
+  kModeDone = 0,       // token already decided (greedy, unusable row)
+  kModeResidual = 1,   // draw from [p - q]_+ of sample_row
+  kModeP = 2,          // draw from p of sample_row (bonus)
+  kModePExcl = 3,      // draw from p of sample_row with the excluded tokens zeroed
+  kModeNoCommit = 4    // bad layout: nothing to do
+};
+
+struct ReqState {
+  int32_t r;
+  int32_t sample_row;
+  int32_t mode;
+  int32_t bonus;
+  uint32_t status;
+  int32_t n_excl;
+  int32_t pad0;
+  int32_t pad1;
+};
+static_assert(sizeof(ReqState) == 32, "ReqState layout");
+
+// Elements per sampling tile (one warp, eight elements per lane).
+constexpr int kTile = 256;
+// Upper bound on the row-statistics grid (partial slots are sized for it).
+constexpr int kMaxStatsGrid = 4096;
+// Upper bound on tree nodes per request.
+constexpr int kMaxNodes = 1024;
+
+struct WsLayout {
+  size_t row_cnt, chunk_cnt, done_cnt, counters_end;
+  size_t rowstat, partial, state, excl, tsum, total;
+  int32_t ntiles;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len) {
+  WsLayout L{};
+  size_t off = 0;
+  L.row_cnt = off;
+  off += sizeof(uint32_t) * static_cast<size_t>(rows > 0 ? rows : 1);
+  L.chunk_cnt = off;
+  off += sizeof(uint32_t) * static_cast<size_t>(batch > 0 ? batch : 1);
+  L.done_cnt = off;
+  off += sizeof(uint32_t) * 4;
+  L.counters_end = off = align_up(off, 256);
+  L.rowstat = off;
+  off = align_up(off + sizeof(RowStat) * static_cast<size_t>(rows > 0 ? rows : 1), 256);
+  L.partial = off;
+  off = align_up(off + sizeof(RowPartial) * 2 * kMaxStatsGrid, 256);
+  L.state = off;
+  off = align_up(off + sizeof(ReqState) * static_cast<size_t>(batch > 0 ? batch : 1), 256);
+  L.excl = off;
+  off = align_up(off + sizeof(int32_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
+                           static_cast<size_t>(max_len > 0 ? max_len : 1), 256);
+  L.ntiles = (vocab + kTile - 1) / kTile;
+  L.tsum = off;
+  off = align_up(off + sizeof(double) * static_cast<size_t>(batch > 0 ? batch : 1) *
+                           static_cast<size_t>(L.ntiles > 0 ? L.ntiles : 1), 256);
+  L.total = off;
+  return L;
+}
+
+// Workspace pointers carved from the caller's buffer.
+struct Ws {
+  uint32_t* row_cnt;
+  uint32_t* chunk_cnt;
+  uint32_t* done_cnt;
+  RowStat* rowstat;
+  RowPartial* partial;
+  ReqState* state;
+  int32_t* excl;
+  double* tsum;
+  int32_t ntiles;
+};
+
+// How the statistics kernel finds a row's temperature.
+enum RowMapKind : int32_t {
+  kMapGreedy = 0,     // every row greedy (no exponentials)
+  kMapFixed = 1,      // request = row / rows_per_req, T = temperature[request]
+  kMapCu = 2,         // request from cu_seqlens (upper bound search), T = temperature[request]
+  kMapPerRow = 3      // T = temperature[row]
+};
+
+struct RowMap {
+  int32_t kind;
+  int32_t rows_per_req;
+  int32_t batch;
+  const int32_t* cu;
+  const float* temperature;
+};
+
+struct LogitsView {
+  const void* base;
+  int32_t dtype;  // SV_F32 or SV_BF16
+  int64_t ld;
+  int64_t rows;
+  int32_t vocab;
+};
+
+struct OutView {
+  int32_t* accept_len;
+  int32_t* num_out;
+  int32_t* out_tokens;
+  int32_t* bonus;
+  int32_t* accept_rows;
+  int32_t* commit_cu;
+  int64_t* commit_src_slot;
+  int64_t* commit_dst_pos;
+  uint32_t* dev_status;
+};
+
+struct ChainParams {
+  LogitsView lg;
+  int32_t batch;
+  int32_t max_len;
+  int32_t fixed_len;          // > 0: request b owns rows [b*fixed_len, (b+1)*fixed_len)
+  const int32_t* cu;          // otherwise cu_seqlens [B+1]
+  const int32_t* ids;
+  const float* q;
+  int64_t ldq;
+  const float* temperature;   // NULL: greedy for every request
+  const float* u_accept;
+  const float* u_final;
+};
+
+struct TreeParams {
+  LogitsView lg;
+  int32_t batch;
+  int32_t nodes;
+  const int32_t* tokens;
+  const int32_t* parents;
+  const int32_t* first_child;   // NULL or [B, nodes]
+  const int32_t* next_sibling;  // NULL or [B, nodes]
+  const float* temperature;     // NULL: greedy
+  float th_single;
+  float th_acc;
+  const float* u_accept;
+  const float* u_final;
+};
+
+struct CommitParams {
+  int32_t batch;
+  int32_t max_len;
+  const int64_t* row_slots;
+  const int64_t* seq_lens;
+};
+
+// Device properties cached per device.
+struct DeviceInfo {
+  int sms;
+  int stats_blocks_per_sm[2];  // [dtype]
+};
+cudaError_t device_info(DeviceInfo* info);
+
+// Launchers (each enqueues on `stream` and returns the launch error).
+cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream);
+int stats_grid(const DeviceInfo& dev, const LogitsView& lg);
+cudaError_t stats_occupancy(int dtype, int* blocks_per_sm);
+
+cudaError_t launch_accept_chain(const ChainParams& p, const OutView& out, const Ws& ws, cudaStream_t stream);
+cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws& ws, cudaStream_t stream);
+
+// Residual / bonus sampler (two passes) followed by the commit, or the commit alone.
+cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
+                                     const OutView& out, const CommitParams& cp, const Ws& ws,
+                                     const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream);
+
+// Row statistics exported as plain arrays.
+cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,
+                                int32_t* out_argmax, double* out_z, float* out_p, uint32_t* row_flags,
+                                cudaStream_t stream);
+
+}  // namespace sv

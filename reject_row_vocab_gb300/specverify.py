@@ -1,0 +1,255 @@
+"""Python binding of libspecverify (ctypes; argument marshalling only).
+
+Every step of the verification runs in the CUDA library; this module only
+turns torch tensors into device pointers and sizes, calls the C ABI declared
+in include/specverify.h on the current torch stream, and raises on a bad
+status.  The library must be built (reject_row_vocab_gb300._build.build());
+importing this module without it raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SV_F32, SV_BF16 = 0, 1
+STATUS = {0: "SV_OK", 1: "SV_ERR_NULL_ARG", 2: "SV_ERR_BAD_SHAPE", 3: "SV_ERR_BAD_DTYPE", 4: "SV_ERR_MISALIGNED",
+          5: "SV_ERR_UNSUPPORTED", 6: "SV_ERR_WORKSPACE_TOO_SMALL", 7: "SV_ERR_CUDA"}
+DEV_TOKEN_RANGE, DEV_NONFINITE, DEV_BAD_TREE, DEV_BAD_LAYOUT, DEV_RESIDUAL_EMPTY, DEV_DUP_SIBLING = 1, 2, 4, 8, 16, 32
+
+ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spec_verify_greedy_chain",
+                "spec_verify_greedy_tree", "spec_verify_rejection_chain", "spec_verify_rejection_ragged",
+                "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__("%s returned %s (%d): %s" % (fn, STATUS.get(code, "?"), code, msg))
+        self.code = code
+
+
+class SvOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "accept_len", "num_out", "out_tokens", "bonus", "accept_rows", "commit_cu", "commit_src_slot",
+        "commit_dst_pos", "dev_status")]
+
+
+_lib = None
+
+
+def load_library():
+    """Load libspecverify.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libspecverify.so is not built (%s); run reject_row_vocab_gb300._build.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    OUT = ctypes.POINTER(SvOut)
+    sig = {
+        "spec_verify_workspace_bytes": ([I64, I32, I32, I32], SZ),
+        "spec_verify_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "spec_verify_greedy_chain": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, OUT, P, SZ, P], ctypes.c_int),
+        "spec_verify_greedy_tree": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, P, P, P, OUT, P, SZ, P],
+                                    ctypes.c_int),
+        "spec_verify_rejection_chain": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, I64, P, P, P, P, P, OUT, P, SZ,
+                                         P], ctypes.c_int),
+        "spec_verify_rejection_ragged": ([P, ctypes.c_int, I64, I32, I64, I32, I32, P, P, P, I64, P, P, P, P, P,
+                                          OUT, P, SZ, P], ctypes.c_int),
+        "spec_verify_target_only_tree": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, P, P, F, F, P, P, P, P,
+                                          OUT, P, SZ, P], ctypes.c_int),
+        "spec_verify_row_stats": ([P, ctypes.c_int, I64, I64, I32, P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
+        "spec_verify_set_stats_events": ([P, P], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype(logits: torch.Tensor) -> int:
+    if logits.dtype == torch.bfloat16:
+        return SV_BF16
+    if logits.dtype == torch.float32:
+        return SV_F32
+    raise TypeError("logits must be bfloat16 or float32, got %s" % logits.dtype)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise SpecVerifyError(fn, code, load_library().spec_verify_status_string(code).decode())
+
+
+def set_stats_events(start=None, stop=None):
+    """Record torch CUDA events around the row-statistics kernel of later calls (None, None: stop).
+
+    The events must already exist on the device (record them once first)."""
+    h = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    _check("spec_verify_set_stats_events", load_library().spec_verify_set_stats_events(h(start), h(stop)))
+
+
+def workspace_bytes(rows: int, batch: int, vocab: int, max_len: int) -> int:
+    return int(load_library().spec_verify_workspace_bytes(rows, batch, vocab, max_len))
+
+
+def workspace(rows: int, batch: int, vocab: int, max_len: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (the library keeps its counters zero between calls)."""
+    n = workspace_bytes(rows, batch, vocab, max_len)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+@dataclass
+class VerifyOutputs:
+    accept_len: torch.Tensor
+    num_out: torch.Tensor
+    out_tokens: torch.Tensor
+    bonus: torch.Tensor
+    accept_rows: torch.Tensor
+    commit_cu: torch.Tensor
+    commit_src_slot: Optional[torch.Tensor]
+    commit_dst_pos: Optional[torch.Tensor]
+    dev_status: torch.Tensor  # int32 storage of uint32 bits
+
+    @staticmethod
+    def allocate(batch: int, max_len: int, rows: int, device=None, slots: bool = True) -> "VerifyOutputs":
+        d = device or "cuda"
+        i32 = dict(dtype=torch.int32, device=d)
+        return VerifyOutputs(
+            accept_len=torch.empty(batch, **i32), num_out=torch.empty(batch, **i32),
+            out_tokens=torch.empty(batch, max_len, **i32), bonus=torch.empty(batch, **i32),
+            accept_rows=torch.empty(batch, max_len, **i32), commit_cu=torch.empty(batch + 1, **i32),
+            commit_src_slot=torch.full((max(rows, 1),), -1, dtype=torch.int64, device=d) if slots else None,
+            commit_dst_pos=torch.full((max(rows, 1),), -1, dtype=torch.int64, device=d) if slots else None,
+            dev_status=torch.empty(batch, **i32))
+
+    def struct(self) -> SvOut:
+        return SvOut(*[None if getattr(self, n) is None else getattr(self, n).data_ptr() for n, _ in SvOut._fields_])
+
+    def to_numpy(self) -> dict:
+        out = {}
+        for n, _ in SvOut._fields_:
+            t = getattr(self, n)
+            if t is not None:
+                a = t.cpu().numpy()
+                out["status" if n == "dev_status" else n] = a.view("uint32") if n == "dev_status" else a
+        return out
+
+
+def _prep(out, ws, batch, max_len, rows, vocab, device, slots):
+    if out is None:
+        out = VerifyOutputs.allocate(batch, max_len, rows, device, slots)
+    if ws is None:
+        ws = workspace(rows, batch, vocab, max_len, device)
+    return out, ws
+
+
+def greedy_chain(logits, verify_ids, m, *, row_slots=None, seq_lens=None, out=None, ws=None, stream=None):
+    """Greedy chain verification of logits [batch*(m+1), V]."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch = rows // (m + 1)
+    out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_greedy_chain", lib.spec_verify_greedy_chain(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(row_slots),
+        _ptr(seq_lens), ctypes.byref(st), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def rejection_chain(logits, verify_ids, m, q, temperature, u_accept, u_final, *, row_slots=None, seq_lens=None,
+                    out=None, ws=None, stream=None):
+    """p/q rejection chain verification of logits [batch*(m+1), V] with proposal rows q."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch = rows // (m + 1)
+    out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_rejection_chain", lib.spec_verify_rejection_chain(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(q), q.stride(0),
+        _ptr(temperature), _ptr(u_accept), _ptr(u_final), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def rejection_ragged(logits, cu_seqlens, max_len, verify_ids, q, temperature, u_accept, u_final, *, row_slots=None,
+                     seq_lens=None, out=None, ws=None, stream=None):
+    """Ragged p/q rejection verification; cu_seqlens [B+1] int32 (lengths include the anchor)."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch = cu_seqlens.numel() - 1
+    out, ws = _prep(out, ws, batch, max_len, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_rejection_ragged", lib.spec_verify_rejection_ragged(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, rows, max_len, V, _ptr(cu_seqlens), _ptr(verify_ids),
+        _ptr(q), q.stride(0), _ptr(temperature), _ptr(u_accept), _ptr(u_final), _ptr(row_slots), _ptr(seq_lens),
+        ctypes.byref(st), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def greedy_tree(logits, tokens, parents, *, first_child=None, next_sibling=None, row_slots=None, seq_lens=None,
+                out=None, ws=None, stream=None):
+    """Greedy tree verification; tokens / parents [batch, nodes], logits [batch*nodes, V]."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch, nodes = tokens.shape
+    out, ws = _prep(out, ws, batch, nodes, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_greedy_tree", lib.spec_verify_greedy_tree(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, nodes, V, _ptr(tokens), _ptr(parents),
+        _ptr(first_child), _ptr(next_sibling), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st), _ptr(ws),
+        ws.numel(), _stream(stream)))
+    return out
+
+
+def target_only_tree(logits, tokens, parents, temperature, u_accept, u_final, *, threshold_single=1.0,
+                     threshold_acc=1.0, first_child=None, next_sibling=None, row_slots=None, seq_lens=None, out=None,
+                     ws=None, stream=None):
+    """Target-only tree sampling; u_accept [batch*nodes], u_final [batch]."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch, nodes = tokens.shape
+    out, ws = _prep(out, ws, batch, nodes, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_target_only_tree", lib.spec_verify_target_only_tree(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, nodes, V, _ptr(tokens), _ptr(parents),
+        _ptr(first_child), _ptr(next_sibling), _ptr(temperature), float(threshold_single), float(threshold_acc),
+        _ptr(u_accept), _ptr(u_final), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return out
+
+
+def row_stats(logits, row_temp=None, probe=None, ws=None, stream=None) -> dict:
+    """Row maximum, lowest argmax, Z (fp64), p at probe and flags for every row."""
+    lib = load_library()
+    rows, V = logits.shape
+    d = logits.device
+    res = {"max": torch.empty(rows, dtype=torch.float32, device=d),
+           "argmax": torch.empty(rows, dtype=torch.int32, device=d),
+           "z": torch.empty(rows, dtype=torch.float64, device=d),
+           "p": torch.empty(rows, dtype=torch.float32, device=d) if probe is not None else None,
+           "flags": torch.empty(rows, dtype=torch.int32, device=d)}
+    if ws is None:
+        ws = workspace(rows, 1, V, 1, d)
+    _check("spec_verify_row_stats", lib.spec_verify_row_stats(
+        _ptr(logits), _dtype(logits), logits.stride(0), rows, V, _ptr(row_temp), _ptr(probe), _ptr(res["max"]),
+        _ptr(res["argmax"]), _ptr(res["z"]), _ptr(res["p"]), _ptr(res["flags"]), _ptr(ws), ws.numel(),
+        _stream(stream)))
+    return res

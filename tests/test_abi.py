@@ -1,0 +1,111 @@
+"""The C-ABI library loads and exports every symbol its header declares; host-side
+argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from reject_row_vocab_gb300 import _build, specverify
+    _build.build()
+    return specverify.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\*?\s+\*?(spec_verify_[a-z_]+)\s*\(",
+                                 text, re.M)))
+
+
+def test_header_declares_the_five_entry_points():
+    names = declared_functions()
+    for n in ("spec_verify_greedy_chain", "spec_verify_greedy_tree", "spec_verify_rejection_chain",
+              "spec_verify_rejection_ragged", "spec_verify_target_only_tree"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from reject_row_vocab_gb300 import specverify
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(specverify.ENTRY_POINTS) <= set(names)
+
+
+def test_status_strings_and_workspace_size(lib):
+    for code in range(8):
+        assert lib.spec_verify_status_string(code)
+    small = lib.spec_verify_workspace_bytes(5, 1, 32000, 5)
+    big = lib.spec_verify_workspace_bytes(1024, 64, 151936, 16)
+    assert 0 < small < big
+    assert big % 256 == 0
+
+
+def _out_struct(addr=0x10000):
+    from reject_row_vocab_gb300.specverify import SvOut
+    return SvOut(*([addr] * 9))
+
+
+def test_host_validation_without_gpu(lib):
+    """Argument errors return before anything is enqueued, so they need no device."""
+    P = ctypes.c_void_p
+    fake = P(0x100000)  # aligned, never dereferenced on the host
+    out = _out_struct()
+    null = None
+    ws = P(0x200000)
+    # NULL logits
+    assert lib.spec_verify_greedy_chain(null, 1, 64, 2, 3, 64, fake, null, null, ctypes.byref(out), ws, 1 << 30,
+                                        null) == 1
+    # bad dtype
+    assert lib.spec_verify_greedy_chain(fake, 7, 64, 2, 3, 64, fake, null, null, ctypes.byref(out), ws, 1 << 30,
+                                        null) == 3
+    # ld < vocab
+    assert lib.spec_verify_greedy_chain(fake, 1, 32, 2, 3, 64, fake, null, null, ctypes.byref(out), ws, 1 << 30,
+                                        null) == 2
+    # misaligned base pointer and row stride
+    assert lib.spec_verify_greedy_chain(P(0x100002), 1, 64, 2, 3, 64, fake, null, null, ctypes.byref(out), ws,
+                                        1 << 30, null) == 4
+    assert lib.spec_verify_greedy_chain(fake, 1, 67, 2, 3, 64, fake, null, null, ctypes.byref(out), ws, 1 << 30,
+                                        null) == 4
+    # commit_src_slot requested without row_slots
+    assert lib.spec_verify_greedy_chain(fake, 1, 64, 2, 3, 64, fake, null, null, ctypes.byref(out), ws, 1 << 30,
+                                        null) == 1
+    out2 = _out_struct()
+    out2.commit_src_slot = None
+    out2.commit_dst_pos = None
+    # workspace too small / misaligned
+    assert lib.spec_verify_greedy_chain(fake, 1, 64, 2, 3, 64, fake, null, null, ctypes.byref(out2), ws, 16,
+                                        null) == 6
+    assert lib.spec_verify_greedy_chain(fake, 1, 64, 2, 3, 64, fake, null, null, ctypes.byref(out2), P(0x200010),
+                                        1 << 30, null) == 6
+    # trees: too many nodes, a half-given sibling list, bad threshold
+    assert lib.spec_verify_greedy_tree(fake, 1, 64, 2, 4096, 64, fake, fake, null, null, null, null,
+                                       ctypes.byref(out2), ws, 1 << 30, null) == 2
+    assert lib.spec_verify_greedy_tree(fake, 1, 64, 2, 8, 64, fake, fake, fake, null, null, null,
+                                       ctypes.byref(out2), ws, 1 << 30, null) == 1
+    assert lib.spec_verify_target_only_tree(fake, 1, 64, 2, 8, 64, fake, fake, null, null, fake,
+                                            ctypes.c_float(1.0), ctypes.c_float(0.0), fake, fake, null, null,
+                                            ctypes.byref(out2), ws, 1 << 30, null) == 2
+    # rejection: q missing, q stride misaligned
+    assert lib.spec_verify_rejection_chain(fake, 1, 64, 2, 3, 64, fake, null, 64, fake, fake, fake, null, null,
+                                           ctypes.byref(out2), ws, 1 << 30, null) == 1
+    assert lib.spec_verify_rejection_chain(fake, 1, 64, 2, 3, 64, fake, fake, 65, fake, fake, fake, null, null,
+                                           ctypes.byref(out2), ws, 1 << 30, null) == 4
+    # ragged: max_len < 1
+    assert lib.spec_verify_rejection_ragged(fake, 1, 64, 2, 8, 0, 64, fake, fake, fake, 64, fake, fake, fake, null,
+                                            null, ctypes.byref(out2), ws, 1 << 30, null) == 2
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from reject_row_vocab_gb300 import specverify
+    monkeypatch.setattr(specverify, "_lib", None)
+    monkeypatch.setattr(specverify, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        specverify.load_library()

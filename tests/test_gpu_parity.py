@@ -1,0 +1,249 @@
+"""CUDA path vs the fp64 oracle, element by element, on the same seeded inputs.
+
+Token decisions (argmax, accepted lengths, token ids, commit indices, status
+bits) must be bit-exact on every request whose decisions are not within 1e-6
+of a threshold (those are counted and reported).  Probabilities must agree to
+1e-5 absolute for fp32 logits and 2e-3 for bf16 logits; the tests also hold
+the row normaliser Z to 2e-6 relative.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+from reject_row_vocab_gb300 import _build  # noqa: E402
+from reject_row_vocab_gb300 import workload as wl  # noqa: E402
+from tests.gpu_compare import compare, oracle_outputs  # noqa: E402
+from tests.helpers import chain_workload, tree_workload  # noqa: E402
+
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+_build.build()
+from reject_row_vocab_gb300 import device_workload as dw  # noqa: E402
+from reject_row_vocab_gb300 import specverify as sv  # noqa: E402
+
+REPORT = []
+
+
+def run_gpu(w, use_lists=False, ws=None, out=None):
+    d = dw.DeviceInputs.from_workload(w)
+    if ws is None:
+        ws = dw.workspace_for(w)
+    o = dw.run(w, d, out=out, ws=ws, use_lists=use_lists)
+    torch.cuda.synchronize()
+    return o.to_numpy()
+
+
+def check(w, use_lists=False):
+    g = run_gpu(w, use_lists=use_lists)
+    o = oracle_outputs(w, use_lists=use_lists)
+    res = compare(w, g, o)
+    REPORT.append((w.name, res))
+    return g, o, res
+
+
+# ---------------------------------------------------------------------------
+# Row statistics and probabilities
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,V", [(4, 1), (5, 3), (3, 7), (9, 16), (7, 1000), (33, 4099), (2, 151936),
+                                    (3000, 64), (5, 32000)])
+def test_row_stats_and_probabilities(dtype, rows, V):
+    rng = np.random.default_rng(rows * 1000 + V)
+    x = (rng.standard_normal((rows, V)) * 3).astype(np.float32)
+    if V > 4:
+        x[0, V // 2] = x[0, V // 3] = x[0].max() + 1.0  # tie: lowest index
+    logits = wl.f32_to_bf16_bits(x) if dtype == "bf16" else x
+    T = rng.uniform(0.4, 1.6, rows).astype(np.float32)
+    T[::5] = 0.0  # greedy rows
+    probe = rng.integers(0, V, rows).astype(np.int32)
+    probe[1 % rows] = np.argmax(wl.bf16_bits_to_f32(logits[1 % rows]) if dtype == "bf16" else x[1 % rows])
+    ref = oracle.row_stats(logits, dtype, row_temp=T, probe=probe)
+    t = dw._to_tensor(logits).cuda()
+    r = sv.row_stats(t, row_temp=torch.from_numpy(T).cuda(), probe=torch.from_numpy(probe).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(r["argmax"].cpu().numpy(), ref["argmax"])
+    assert np.array_equal(r["max"].cpu().numpy().astype(np.float64), ref["max"])
+    z = r["z"].cpu().numpy()
+    samp = T > 0
+    assert np.all(z[~samp] == 0)
+    assert np.all(np.abs(z[samp] - ref["z"][samp]) <= 2e-6 * ref["z"][samp])
+    p = r["p"].cpu().numpy().astype(np.float64)
+    tol = 1e-5 if dtype == "f32" else 2e-3
+    assert np.all(np.abs(p - ref["p"]) <= tol)
+    assert np.all(np.abs(p - ref["p"]) <= 2e-6 * np.maximum(ref["p"], 1e-30) + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Small cases spanning several tiles and a ragged tail
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 16, 1000, 4099, 32000])
+def test_greedy_chain_small(dtype, V):
+    w = wl.greedy_chain(batch=6, m=5, vocab=V, dtype=dtype, p_match=0.8, seed=V)
+    check(w)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [2, 7, 16, 1000, 4099, 20011])
+def test_rejection_chain_small(dtype, V):
+    w = wl.rejection_chain(batch=9, m=6, vocab=V, dtype=dtype, boost=2.0, temperature=0.9, noise_sigma=0.7,
+                           seed=V + 1)
+    check(w)
+
+
+@pytest.mark.parametrize("V", [3, 999, 7777])
+def test_ragged_small(V):
+    w = wl.ragged_block(batch=40, max_len=8, vocab=V, seed=V + 2)
+    check(w)
+    w1 = wl.ragged_block(lens=[1, 1, 3, 1, 8], max_len=8, vocab=V, seed=V + 3)  # bonus-only requests
+    check(w1)
+
+
+@pytest.mark.parametrize("mode", ["greedy_tree", "target_only_tree"])
+@pytest.mark.parametrize("V,keep", [(64, 6), (2000, 16), (5003, 30)])
+def test_tree_small(mode, V, keep):
+    w = wl.eagle2_tree(batch=12, topk=3, depth=4, keep=keep, vocab=V, mode=mode, noise_sigma=0.5,
+                       temperature=0.9, seed=V + keep)
+    check(w)
+    w.first_child, w.next_sibling = wl.sibling_lists(w.parents)
+    check(w, use_lists=True)
+
+
+def test_chain_and_tree_entry_points_agree():
+    w = wl.greedy_chain(batch=20, m=7, vocab=3000, dtype="bf16", p_match=0.85, seed=5)
+    L = 8
+    t = tree_workload(w.logits, "bf16", w.verify_ids.reshape(20, L), np.tile(np.arange(-1, L - 1), (20, 1)))
+    g1 = run_gpu(w)
+    g2 = run_gpu(t)
+    for k in ("accept_len", "num_out", "out_tokens", "bonus", "accept_rows", "commit_cu"):
+        assert np.array_equal(g1[k], g2[k]), k
+
+
+# ---------------------------------------------------------------------------
+# The five workloads at full size (the launch configuration the benchmark times)
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("idx,mode", [(1, None), (2, None), (3, "greedy_tree"), (3, "target_only_tree"), (4, None),
+                                      (5, None)])
+def test_full_size_configs(idx, mode):
+    w = wl.config(idx, mode=mode) if mode else wl.config(idx)
+    g, o, res = check(w)
+    assert res["flagged"] <= max(1, w.batch // 50)
+    # accepted lengths stay within [0, max_len - 1]; tau = E[r + 1] within [1, k + 1]
+    assert np.all((g["accept_len"] >= 0) & (g["accept_len"] < w.max_len))
+
+
+# ---------------------------------------------------------------------------
+# Degenerate inputs
+# ---------------------------------------------------------------------------
+
+
+def test_nonfinite_and_unusable_rows():
+    V = 300
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((8, V)).astype(np.float32)
+    x[0, 5] = np.nan
+    x[0, 9] = np.inf
+    x[1, :] = -np.inf
+    x[4, 100] = -np.inf
+    x[5, :] = -np.inf
+    x[5, 17] = np.nan
+    ids = rng.integers(0, V, 8).astype(np.int32)
+    ids[1] = int(np.nanargmax(np.where(np.isfinite(x[0]), x[0], -np.inf)))
+    for dtype in ("f32", "bf16"):
+        lg = wl.f32_to_bf16_bits(x) if dtype == "bf16" else x
+        check(chain_workload(lg, dtype, [0, 4, 8], ids, name="nonfinite_" + dtype))
+        q = np.full((8, V), 1.0 / V, np.float32)
+        check(chain_workload(lg, dtype, [0, 4, 8], ids, q=q, T=[1.0, 0.7], ua=np.full(8, 0.3), uf=[0.2, 0.9],
+                             name="nonfinite_rej_" + dtype))
+
+
+def test_bad_layouts_and_token_ranges():
+    V = 500
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal((12, V)) * 2).astype(np.float32)
+    ids = rng.integers(0, V, 12).astype(np.int32)
+    ids[1] = -5
+    ids[7] = V + 3
+    q = np.full((12, V), 1.0 / V, np.float32)
+    for cu in ([0, 3, 2, 12], [0, 4, 8, 13], [0, 12, 12, 12], [0, 1, 2, 3]):
+        w = chain_workload(x, "f32", cu, ids, q=q, T=[1.0, 1.0, 0.0], ua=np.full(12, 0.5), uf=[0.1, 0.5, 0.9],
+                           max_len=6, name="bad_cu")
+        check(w)
+
+
+def test_empty_batch():
+    d = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
+    o = sv.greedy_chain(d, torch.zeros(0, dtype=torch.int32, device="cuda"), 3)
+    torch.cuda.synchronize()
+    assert o.commit_cu.cpu().tolist() == [0]
+
+
+def test_single_row_requests_and_m_zero():
+    w = wl.rejection_chain(batch=17, m=0, vocab=3001, dtype="bf16", seed=8)
+    g, o, _ = check(w)
+    assert np.all(g["accept_len"] == 0) and np.all(g["num_out"] == 1)
+    check(wl.greedy_chain(batch=5, m=0, vocab=100, dtype="f32", seed=9))
+
+
+def test_q_equal_p_accepts_everything():
+    V = 700
+    rng = np.random.default_rng(4)
+    B, L = 10, 5
+    x = (rng.standard_normal((B * L, V)) * 2).astype(np.float32)
+    T = 0.8
+    p = np.exp((x - x.max(1, keepdims=True)) / np.float32(T))
+    p /= p.sum(1, keepdims=True)
+    ids = rng.integers(0, V, B * L).astype(np.int32)
+    w = chain_workload(x, "f32", np.arange(B + 1) * L, ids, q=p.astype(np.float32), T=np.full(B, T),
+                       ua=np.minimum(wl.uniforms(rng, B * L), 0.999), uf=wl.uniforms(rng, B))
+    g, o, _ = check(w)
+    assert np.all(g["accept_len"] == L - 1)
+
+
+def test_invalid_trees_and_duplicate_siblings():
+    V, N, B = 50, 6, 4
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((B * N, V)) * 2).astype(np.float32)
+    par = np.tile(np.array([-1, 0, 0, 1, 1, 2], np.int32), (B, 1))
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    par[1, 3] = 4  # forward parent: invalid
+    par[2, 0] = 0  # root with a parent: invalid
+    tok[3, 2] = tok[3, 1]  # duplicate siblings
+    tok[0, 1] = int(np.argmax(x[0]))
+    tok[3, 1] = int(np.argmax(x[3 * N]))
+    tok[3, 2] = tok[3, 1]
+    for kind in ("greedy_tree", "target_only_tree"):
+        w = tree_workload(x, "f32", tok, par, T=np.full(B, 0.9), ua=wl.uniforms(rng, B * N), uf=wl.uniforms(rng, B),
+                          kind=kind)
+        check(w)
+
+
+def test_workspace_reuse_gives_identical_results():
+    w = wl.ragged_block(batch=64, max_len=8, vocab=5000, seed=11)
+    d = dw.DeviceInputs.from_workload(w)
+    ws = dw.workspace_for(w)
+    first = dw.run(w, d, ws=ws).to_numpy()
+    for _ in range(3):
+        again = dw.run(w, d, ws=ws).to_numpy()
+        for k in first:
+            assert np.array_equal(first[k], again[k]), k
+    n = sv.workspace_bytes(w.rows, w.batch, w.vocab, w.max_len)
+    assert int(ws[: n].sum().item()) != 0  # scratch is in use, counters were reset by the kernels
+
+
+def test_report_flagged_counts():
+    """Reports how many requests fell within 1e-6 of a decision threshold."""
+    tot = sum(r["requests"] for _, r in REPORT)
+    fl = sum(r["flagged"] for _, r in REPORT)
+    print("\nparity report: %d requests compared, %d flagged near a threshold, %d of those differ"
+          % (tot, fl, sum(r["differ_flagged"] for _, r in REPORT)))
