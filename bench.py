@@ -30,8 +30,8 @@ if ROOT not in sys.path:
 
 METRIC = "verified rows/s"
 UNIT = "rows/s"
-KERNELS_PER_STEP = {"greedy_chain": 3, "greedy_tree": 3, "rejection_chain": 4, "rejection_ragged": 4,
-                    "target_only_tree": 4}
+KERNELS_PER_STEP = {"greedy_chain": 3, "greedy_tree": 3, "rejection_chain": 3, "rejection_ragged": 3,
+                    "target_only_tree": 3}
 STATS_SOURCES = ("reject_row_vocab_gb300/csrc/sv_stats.cu", "reject_row_vocab_gb300/csrc/sv_device.cuh")
 
 

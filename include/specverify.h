@@ -74,6 +74,8 @@ typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype_t;
 #define SV_DEV_BAD_LAYOUT 8u     /* cu_seqlens range invalid: nothing committed, num_out 0, bonus -1      */
 #define SV_DEV_RESIDUAL_EMPTY 16u /* residual mass was <= 0: the token was sampled from p instead         */
 #define SV_DEV_DUP_SIBLING 32u   /* target-only tree: a sibling repeats a token; the repeat is skipped    */
+#define SV_DEV_TIMEOUT 64u       /* a bounded wait inside a kernel gave up (never expected): this call's   */
+                                 /* outputs are undefined and the workspace must be zero-filled again      */
 
 /*
  * Outputs of one call (all DEVICE pointers, caller-owned).  max_len is the
@@ -99,6 +101,10 @@ size_t spec_verify_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, i
 
 /* Static description of a status code. */
 const char* spec_verify_status_string(sv_status_t status);
+
+/* Description of the CUDA error behind the last SV_ERR_CUDA returned on this
+ * host thread ("no error" if none). */
+const char* spec_verify_last_cuda_error(void);
 
 /* Benchmark instrumentation (not needed for verification).  While set, every
  * call made from this host thread records `start` on its stream immediately

@@ -69,48 +69,62 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
 
   const float T = p.temperature ? p.temperature[b] : 0.0f;
   const bool greedy = !sampling_temperature(T);
-  uint32_t st = 0u;
+  uint32_t st = __ldcg(ws.err) ? kStTimeout : 0u;
   int64_t s = L - 1;  // row (within the request) that yields the final token
   int how = 0;        // 0 all accepted, 1 rejected, 2 unusable row
-  for (int64_t j0 = 0; j0 < L - 1; j0 += 32) {
+  RowStat fs{};
+  // Each lane takes one row (the last row too, for its statistics): the
+  // statistics and the tested id load together, then the two gathers.
+  for (int64_t j0 = 0; j0 < L; j0 += 32) {
     const int64_t j = j0 + lane;
-    const bool active = j < L - 1;
+    const bool has_row = j < L;
+    const bool tested = j < L - 1;
+    const int64_t row = start + j;
+    RowStat rs{};
+    int32_t d = -1;
+    if (has_row) rs = ws.rowstat[row];
+    if (tested) d = p.ids[row + 1];
     int stop = 0;
-    uint32_t fl = 0u;
-    if (active) {
-      const int64_t row = start + j;
-      const RowStat rs = ws.rowstat[row];
-      fl = rs.flags;
+    uint32_t fl = rs.flags;
+    if (tested) {
       if (rs.argmax < 0) {
         stop = 2;
         fl |= kStNonFinite;
+      } else if (d < 0 || d >= p.lg.vocab) {
+        stop = 1;
+        fl |= kStTokenRange;
+      } else if (greedy) {
+        stop = (rs.argmax != d) ? 1 : 0;
       } else {
-        const int32_t d = p.ids[row + 1];
-        if (d < 0 || d >= p.lg.vocab) {
-          stop = 1;
-          fl |= kStTokenRange;
-        } else if (greedy) {
-          stop = (rs.argmax != d) ? 1 : 0;
-        } else {
-          const double pd = target_prob(p.lg, row, d, rs);
-          const double qd = static_cast<double>(p.q[row * p.ldq + d]);
-          const double u = static_cast<double>(p.u_accept[row]);
-          stop = (u * qd < pd) ? 0 : 1;
-        }
+        const float l = load_logit(p.lg, row, d);
+        const double qd = static_cast<double>(p.q[row * p.ldq + d]);
+        const double pd = usable_logit(l) ? static_cast<double>(exp2f((l - rs.M) * rs.k)) / rs.Z : 0.0;
+        const double u = static_cast<double>(p.u_accept[row]);
+        stop = (u * qd < pd) ? 0 : 1;
       }
     }
-    const unsigned bal = __ballot_sync(kFull, active && stop != 0);
+    const unsigned bal = __ballot_sync(kFull, tested && stop != 0);
     const int first = bal ? __ffs(bal) - 1 : 32;
-    st |= warp_or((active && lane <= first) ? fl : 0u);  // rows past the stop are not visited
+    st |= warp_or((tested && lane <= first) ? fl : 0u);  // rows past the stop are not visited
+    int src = -1;
     if (bal) {
       s = j0 + first;
       how = __shfl_sync(kFull, stop, first);
+      src = first;
+    } else if (L - 1 - j0 < 32) {
+      src = static_cast<int>(L - 1 - j0);  // every draft passed: the last row gives the bonus
+    }
+    if (src >= 0) {
+      fs.Z = __shfl_sync(kFull, rs.Z, src);
+      fs.M = __shfl_sync(kFull, rs.M, src);
+      fs.argmax = __shfl_sync(kFull, rs.argmax, src);
+      fs.flags = __shfl_sync(kFull, rs.flags, src);
+      fs.k = __shfl_sync(kFull, rs.k, src);
       break;
     }
   }
 
   const int64_t fr = start + s;
-  const RowStat fs = ws.rowstat[fr];
   st |= fs.flags;
   int32_t bonus = -1;
   int32_t mode = kModeDone;
@@ -188,7 +202,7 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
 
   const float T = p.temperature ? p.temperature[b] : 0.0f;
   const bool greedy = !sampling_temperature(T);
-  uint32_t st = bad ? kStBadTree : 0u;
+  uint32_t st = (bad ? kStBadTree : 0u) | (__ldcg(ws.err) ? kStTimeout : 0u);
   int cur = 0, depth = 0;
   int32_t bonus = -1;
   int32_t mode = kModeDone;

@@ -32,6 +32,8 @@ cudaError_t device_info(DeviceInfo* info) {
     if (e != cudaSuccess) return e;
     e = stats_occupancy(SV_BF16, &d.stats_blocks_per_sm[1]);
     if (e != cudaSuccess) return e;
+    e = sample_smem_setup();
+    if (e != cudaSuccess) return e;
     if (d.stats_blocks_per_sm[0] < 1) d.stats_blocks_per_sm[0] = 1;
     if (d.stats_blocks_per_sm[1] < 1) d.stats_blocks_per_sm[1] = 1;
     cache[dev] = d;
@@ -78,6 +80,7 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   w->row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
   w->chunk_cnt = reinterpret_cast<uint32_t*>(base + L.chunk_cnt);
   w->done_cnt = reinterpret_cast<uint32_t*>(base + L.done_cnt);
+  w->err = w->done_cnt + 1;
   w->rowstat = reinterpret_cast<RowStat*>(base + L.rowstat);
   w->partial = reinterpret_cast<RowPartial*>(base + L.partial);
   w->state = reinterpret_cast<ReqState*>(base + L.state);
@@ -98,16 +101,28 @@ sv_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ER
 thread_local cudaEvent_t t_stats_start = nullptr;
 thread_local cudaEvent_t t_stats_stop = nullptr;
 
+// While a stream is being captured into a graph, an external record becomes an
+// event node of the graph; otherwise a plain record.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+  return cudaEventRecord(ev, stream);
+}
+
 cudaError_t row_stats_timed(const LogitsView& lg, const RowMap& map, const Ws& w, int grid, cudaStream_t stream) {
   cudaError_t e;
-  if (t_stats_start && (e = cudaEventRecord(t_stats_start, stream)) != cudaSuccess) return e;
+  if (t_stats_start && (e = record_event(t_stats_start, stream)) != cudaSuccess) return e;
   e = launch_row_stats(lg, map, w, grid, stream);
   if (e != cudaSuccess) return e;
-  if (t_stats_stop) return cudaEventRecord(t_stats_stop, stream);
+  if (t_stats_stop) return record_event(t_stats_stop, stream);
   return cudaSuccess;
 }
 
+// An empty batch commits nothing: commit_cu = [0].  Every other pointer may be NULL.
 sv_status_t empty_batch(const sv_out_t* out, cudaStream_t stream) {
+  if (!out || !out->commit_cu) return SV_ERR_NULL_ARG;
   return cuda_status(cudaMemsetAsync(out->commit_cu, 0, sizeof(int32_t), stream));
 }
 
@@ -116,10 +131,15 @@ sv_status_t empty_batch(const sv_out_t* out, cudaStream_t stream) {
     const sv_status_t _s = (expr);        \
     if (_s != SV_OK) return _s;           \
   } while (0)
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
 #define SV_TRY_CUDA(expr)                 \
   do {                                    \
     const cudaError_t _e = (expr);        \
-    if (_e != cudaSuccess) return SV_ERR_CUDA; \
+    if (_e != cudaSuccess) {              \
+      t_last_cuda_error = _e;             \
+      return SV_ERR_CUDA;                 \
+    }                                     \
   } while (0)
 
 }  // namespace
@@ -140,6 +160,8 @@ sv_status_t spec_verify_set_stats_events(cudaEvent_t start, cudaEvent_t stop) {
   return SV_OK;
 }
 
+const char* spec_verify_last_cuda_error(void) { return cudaGetErrorString(t_last_cuda_error); }
+
 const char* spec_verify_status_string(sv_status_t status) {
   switch (status) {
     case SV_OK: return "ok";
@@ -159,11 +181,11 @@ sv_status_t spec_verify_greedy_chain(const void* logits, sv_dtype_t dtype, int64
                                      const int64_t* seq_lens, const sv_out_t* out, void* ws, size_t ws_bytes,
                                      cudaStream_t stream) {
   if (batch < 0 || m < 0 || m >= (1 << 20)) return SV_ERR_BAD_SHAPE;
+  if (batch == 0) return empty_batch(out, stream);
   const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
   SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
   if (!verify_ids) return SV_ERR_NULL_ARG;
   SV_TRY(check_out(out, row_slots, seq_lens));
-  if (batch == 0) return empty_batch(out, stream);
   Ws w{};
   SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, m + 1, &w));
   DeviceInfo dev{};
@@ -173,7 +195,7 @@ sv_status_t spec_verify_greedy_chain(const void* logits, sv_dtype_t dtype, int64
   ChainParams p{lg, batch, m + 1, m + 1, nullptr, verify_ids, nullptr, 0, nullptr, nullptr, nullptr};
   const OutView ov = out_view(out);
   SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
-  SV_TRY_CUDA(launch_commit(ov, CommitParams{batch, m + 1, row_slots, seq_lens}, stream));
+  SV_TRY_CUDA(launch_commit(ov, CommitParams{batch, m + 1, row_slots, seq_lens, w.err}, stream));
   return SV_OK;
 }
 
@@ -184,12 +206,12 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
                                     const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
                                     void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (batch > 65535) return SV_ERR_BAD_SHAPE;  // the sampler's grid has one y-slice per request
+  if (batch == 0) return empty_batch(out, stream);
   SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
   if (!verify_ids || !temperature || !u_accept || !u_final) return SV_ERR_NULL_ARG;
   if (fixed_len == 0 && !cu) return SV_ERR_NULL_ARG;
   SV_TRY(check_q(q, ldq, vocab));
   SV_TRY(check_out(out, row_slots, seq_lens));
-  if (batch == 0) return empty_batch(out, stream);
   Ws w{};
   SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w));
   DeviceInfo dev{};
@@ -203,7 +225,7 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
   }
   ChainParams p{lg, batch, max_len, fixed_len, cu, verify_ids, q, ldq, temperature, u_accept, u_final};
   SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
-  SV_TRY_CUDA(launch_sample_and_commit(lg, q, ldq, u_final, ov, CommitParams{batch, max_len, row_slots, seq_lens}, w,
+  SV_TRY_CUDA(launch_sample_and_commit(lg, q, ldq, u_final, ov, CommitParams{batch, max_len, row_slots, seq_lens, w.err}, w,
                                        dev, stream));
   return SV_OK;
 }
@@ -238,6 +260,7 @@ static sv_status_t tree_common(int mode, const void* logits, sv_dtype_t dtype, i
                                const float* u_final, const int64_t* row_slots, const int64_t* seq_lens,
                                const sv_out_t* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (batch < 0 || nodes < 1 || nodes > kMaxNodes || (mode == 1 && batch > 65535)) return SV_ERR_BAD_SHAPE;
+  if (batch == 0) return empty_batch(out, stream);
   const int64_t rows = static_cast<int64_t>(batch) * nodes;
   SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
   if (!tokens || !parents) return SV_ERR_NULL_ARG;
@@ -248,7 +271,6 @@ static sv_status_t tree_common(int mode, const void* logits, sv_dtype_t dtype, i
       return SV_ERR_BAD_SHAPE;
   }
   SV_TRY(check_out(out, row_slots, seq_lens));
-  if (batch == 0) return empty_batch(out, stream);
   Ws w{};
   SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, nodes, &w));
   DeviceInfo dev{};
@@ -265,7 +287,7 @@ static sv_status_t tree_common(int mode, const void* logits, sv_dtype_t dtype, i
                threshold_single, threshold_acc,
                u_accept,    u_final};
   SV_TRY_CUDA(launch_accept_tree(p, ov, w, stream));
-  const CommitParams cp{batch, nodes, row_slots, seq_lens};
+  const CommitParams cp{batch, nodes, row_slots, seq_lens, w.err};
   if (mode == 1) {
     SV_TRY_CUDA(launch_sample_and_commit(lg, nullptr, 0, u_final, ov, cp, w, dev, stream));
   } else {
@@ -311,6 +333,7 @@ sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t 
                               : RowMap{kMapGreedy, 1, 0, nullptr, nullptr};
   SV_TRY_CUDA(row_stats_timed(lg, map, w, stats_grid(dev, lg), stream));
   SV_TRY_CUDA(launch_export_stats(lg, w, probe, out_max, out_argmax, out_z, out_p, row_flags, stream));
+  SV_TRY_CUDA(cudaMemsetAsync(w.err, 0, sizeof(uint32_t), stream));
   return SV_OK;
 }
 

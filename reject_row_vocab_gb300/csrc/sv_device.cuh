@@ -41,6 +41,77 @@ __device__ __forceinline__ float load_logit(const LogitsView& lg, int64_t row, i
 }
 
 // ---------------------------------------------------------------------------
+// Bulk copies (TMA engine) and mbarriers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity, for at most `limit_ns`;
+// gives up early once *abort is set.  Returns false if it gave up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spin & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// One bulk copy global -> shared, completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+// Barrier among the first `threads` threads of the block (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int threads) { asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); }
+
+// ---------------------------------------------------------------------------
 // Arithmetic helpers
 // ---------------------------------------------------------------------------
 
@@ -78,14 +149,15 @@ __device__ __forceinline__ bool sampling_temperature(float T) { return (T >= 1e-
 // Partial row statistics: (m, s, idx, flags) with s = sum 2^((l - m) k)
 // ---------------------------------------------------------------------------
 
+// In-CTA partial (fp32).  Merged in double only across CTAs.
 struct Part {
   float m;
-  double s;
+  float s;
   int32_t idx;
   uint32_t flags;
 };
 
-__device__ __forceinline__ Part part_identity() { return Part{-kInfF, 0.0, -1, 0u}; }
+__device__ __forceinline__ Part part_identity() { return Part{-kInfF, 0.0f, -1, 0u}; }
 
 // Merge b into a.  The larger maximum wins its index; equal maxima keep the
 // lower index; sums are rescaled to the common maximum (exactly 1 for the
@@ -100,18 +172,11 @@ __device__ __forceinline__ void part_merge(Part& a, const Part& b, float k) {
   } else {
     idx = min(a.idx, b.idx);
   }
-  double s = 0.0;
+  float s = 0.0f;
   if (k > 0.0f && M > -kInfF) {
-    if (a.m == M) {
-      s += a.s;
-    } else if (a.s != 0.0) {
-      s += a.s * static_cast<double>(exp2f((a.m - M) * k));
-    }
-    if (b.m == M) {
-      s += b.s;
-    } else if (b.s != 0.0) {
-      s += b.s * static_cast<double>(exp2f((b.m - M) * k));
-    }
+    const float sa = (a.m == M) ? a.s : (a.s != 0.0f ? a.s * exp2f((a.m - M) * k) : 0.0f);
+    const float sb = (b.m == M) ? b.s : (b.s != 0.0f ? b.s * exp2f((b.m - M) * k) : 0.0f);
+    s = sa + sb;
   }
   a.m = M;
   a.s = s;
@@ -154,9 +219,78 @@ __device__ __forceinline__ Part part_block_reduce(Part p, float k, Part* smem /*
   return p;
 }
 
+// Reduce over the first NT threads (whole warps) with the named barrier; the
+// result is valid in every thread of warp 0.
+template <int NT>
+__device__ __forceinline__ Part part_reduce_named(Part p, float k, Part* smem /* [NT/32] */) {
+  constexpr int NW = NT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  p = part_warp_reduce(p, k);
+  if (lane == 0) smem[warp] = p;
+  named_sync(NT);
+  if (warp == 0) {
+    p = lane < NW ? smem[lane] : part_identity();
+    p = part_warp_reduce(p, k);
+  }
+  named_sync(NT);
+  return p;
+}
+
+// Cross-CTA partial in double: (m, s, idx, flags).
+struct PartD {
+  float m;
+  double s;
+  int32_t idx;
+  uint32_t flags;
+};
+
+__device__ __forceinline__ PartD partd_identity() { return PartD{-kInfF, 0.0, -1, 0u}; }
+
+__device__ __forceinline__ void partd_merge(PartD& a, const PartD& b, float k) {
+  const float M = fmaxf(a.m, b.m);
+  int32_t idx;
+  if (a.m > b.m) {
+    idx = a.idx;
+  } else if (b.m > a.m) {
+    idx = b.idx;
+  } else {
+    idx = min(a.idx, b.idx);
+  }
+  double s = 0.0;
+  if (k > 0.0f && M > -kInfF) {
+    if (a.m == M) {
+      s += a.s;
+    } else if (a.s != 0.0) {
+      s += a.s * static_cast<double>(exp2f((a.m - M) * k));
+    }
+    if (b.m == M) {
+      s += b.s;
+    } else if (b.s != 0.0) {
+      s += b.s * static_cast<double>(exp2f((b.m - M) * k));
+    }
+  }
+  a.m = M;
+  a.s = s;
+  a.idx = idx;
+  a.flags |= b.flags;
+}
+
+__device__ __forceinline__ PartD partd_warp_reduce(PartD p, float k) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    PartD o;
+    o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
+    o.s = __shfl_xor_sync(0xffffffffu, p.s, off);
+    o.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
+    o.flags = __shfl_xor_sync(0xffffffffu, p.flags, off);
+    partd_merge(p, o, k);
+  }
+  return p;
+}
+
 // Coherent (L2) loads of a partial written by another CTA.
-__device__ __forceinline__ Part load_partial_cg(const RowPartial* rp) {
-  Part p;
+__device__ __forceinline__ PartD load_partial_cg(const RowPartial* rp) {
+  PartD p;
   p.s = __ldcg(&rp->s);
   p.m = __ldcg(&rp->m);
   p.idx = __ldcg(&rp->idx);

@@ -20,6 +20,7 @@ constexpr uint32_t kStBadTree = SV_DEV_BAD_TREE;
 constexpr uint32_t kStBadLayout = SV_DEV_BAD_LAYOUT;
 constexpr uint32_t kStResidualEmpty = SV_DEV_RESIDUAL_EMPTY;
 constexpr uint32_t kStDupSibling = SV_DEV_DUP_SIBLING;
+constexpr uint32_t kStTimeout = SV_DEV_TIMEOUT;
 
 // Final statistics of one logits row, written by the row-statistics kernel.
 // M is the row maximum over usable entries (finite or -inf), argmax its lowest
@@ -112,6 +113,7 @@ struct Ws {
   uint32_t* row_cnt;
   uint32_t* chunk_cnt;
   uint32_t* done_cnt;
+  uint32_t* err;  // sticky error word: a bounded wait gave up (reported as SV_DEV_TIMEOUT)
   RowStat* rowstat;
   RowPartial* partial;
   ReqState* state;
@@ -190,6 +192,7 @@ struct CommitParams {
   int32_t max_len;
   const int64_t* row_slots;
   const int64_t* seq_lens;
+  uint32_t* err;  // workspace error word, cleared once the call's statuses carry it
 };
 
 // Device properties cached per device.
@@ -212,6 +215,7 @@ cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
                                      const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream);
+cudaError_t sample_smem_setup();
 
 // Row statistics exported as plain arrays.
 cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,

@@ -33,63 +33,71 @@ __device__ __forceinline__ bool sampling_mode(int32_t mode) {
   return mode == kModeResidual || mode == kModeP || mode == kModePExcl;
 }
 
-// The eight weights of one lane of a tile: entries [col0, col0 + 8) of `row`.
-// Entries past the vocabulary weigh 0.  Both passes call this with the same
-// arguments, so a tile's weights are bit-identical in both.
-__device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
-                                             const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
-                                             int32_t n_excl, int64_t col0, float (&w)[8]) {
-  const int V = lg.vocab;
-  float x[8];
-  if (col0 + 8 <= V) {
-    if (lg.dtype == SV_BF16) {
-      const uint4 r = ld_stream16(static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 2);
-      x[0] = bf16_lo(r.x);
-      x[1] = bf16_hi(r.x);
-      x[2] = bf16_lo(r.y);
-      x[3] = bf16_hi(r.y);
-      x[4] = bf16_lo(r.z);
-      x[5] = bf16_hi(r.z);
-      x[6] = bf16_lo(r.w);
-      x[7] = bf16_hi(r.w);
-    } else {
-      const char* base = static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 4;
-      const uint4 r0 = ld_stream16(base), r1 = ld_stream16(base + 16);
-      x[0] = __uint_as_float(r0.x);
-      x[1] = __uint_as_float(r0.y);
-      x[2] = __uint_as_float(r0.z);
-      x[3] = __uint_as_float(r0.w);
-      x[4] = __uint_as_float(r1.x);
-      x[5] = __uint_as_float(r1.y);
-      x[6] = __uint_as_float(r1.z);
-      x[7] = __uint_as_float(r1.w);
-    }
+// Raw 16-byte loads of one lane's eight entries (logits, and q for a residual).
+struct LaneRaw {
+  uint4 l0, l1, q0, q1;
+};
+
+__device__ __forceinline__ void lane_load_full(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
+                                               bool resid, int64_t col0, LaneRaw& r) {
+  if (lg.dtype == SV_BF16) {
+    r.l0 = ld_stream16(static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 2);
   } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = (col0 + i < V) ? load_logit(lg, row, col0 + i) : -kInfF;
+    const char* base = static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 4;
+    r.l0 = ld_stream16(base);
+    r.l1 = ld_stream16(base + 16);
   }
+  if (resid) {
+    const char* qb = reinterpret_cast<const char*>(q + row * ldq + col0);
+    r.q0 = ld_stream16(qb);
+    r.q1 = ld_stream16(qb + 16);
+  }
+}
+
+__device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, bool resid, float (&x)[8],
+                                            float (&qv)[8]) {
+  if (dtype == SV_BF16) {
+    x[0] = bf16_lo(r.l0.x);
+    x[1] = bf16_hi(r.l0.x);
+    x[2] = bf16_lo(r.l0.y);
+    x[3] = bf16_hi(r.l0.y);
+    x[4] = bf16_lo(r.l0.z);
+    x[5] = bf16_hi(r.l0.z);
+    x[6] = bf16_lo(r.l0.w);
+    x[7] = bf16_hi(r.l0.w);
+  } else {
+    x[0] = __uint_as_float(r.l0.x);
+    x[1] = __uint_as_float(r.l0.y);
+    x[2] = __uint_as_float(r.l0.z);
+    x[3] = __uint_as_float(r.l0.w);
+    x[4] = __uint_as_float(r.l1.x);
+    x[5] = __uint_as_float(r.l1.y);
+    x[6] = __uint_as_float(r.l1.z);
+    x[7] = __uint_as_float(r.l1.w);
+  }
+  if (resid) {
+    qv[0] = __uint_as_float(r.q0.x);
+    qv[1] = __uint_as_float(r.q0.y);
+    qv[2] = __uint_as_float(r.q0.z);
+    qv[3] = __uint_as_float(r.q0.w);
+    qv[4] = __uint_as_float(r.q1.x);
+    qv[5] = __uint_as_float(r.q1.y);
+    qv[6] = __uint_as_float(r.q1.z);
+    qv[7] = __uint_as_float(r.q1.w);
+  }
+}
+
+// Weights of eight entries from their values; the single definition both
+// passes use, so a tile's weights are bit-identical in both.
+__device__ __forceinline__ void weights_from_values(const float (&x)[8], const float (&qv)[8], const RowStat& rs,
+                                                    float inv_z, int32_t mode, const int32_t* excl, int32_t n_excl,
+                                                    int64_t col0, float (&w)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float e = usable_logit(x[i]) ? ex2_fast(__fmul_rn(__fsub_rn(x[i], rs.M), rs.k)) : 0.0f;
     w[i] = __fmul_rn(e, inv_z);
   }
   if (mode == kModeResidual) {
-    float qv[8];
-    if (col0 + 8 <= V) {
-      const char* qb = reinterpret_cast<const char*>(q + row * ldq + col0);
-      const uint4 r0 = ld_stream16(qb), r1 = ld_stream16(qb + 16);
-      qv[0] = __uint_as_float(r0.x);
-      qv[1] = __uint_as_float(r0.y);
-      qv[2] = __uint_as_float(r0.z);
-      qv[3] = __uint_as_float(r0.w);
-      qv[4] = __uint_as_float(r1.x);
-      qv[5] = __uint_as_float(r1.y);
-      qv[6] = __uint_as_float(r1.z);
-      qv[7] = __uint_as_float(r1.w);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = (col0 + i < V) ? __ldg(q + row * ldq + col0 + i) : 0.0f;
-    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = fmaxf(__fsub_rn(w[i], qv[i]), 0.0f);
   } else if (mode == kModePExcl) {
@@ -102,17 +110,51 @@ __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* 
   }
 }
 
-__device__ __forceinline__ double lane_sum(const float (&w)[8]) {
-  double s = 0.0;
+// The eight weights of one lane of a tile: entries [col0, col0 + 8) of `row`.
+// Entries past the vocabulary weigh 0.
+__device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
+                                             const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
+                                             int32_t n_excl, int64_t col0, float (&w)[8]) {
+  const bool resid = mode == kModeResidual;
+  float x[8], qv[8];
+  if (col0 + 8 <= lg.vocab) {
+    LaneRaw r;
+    lane_load_full(lg, q, ldq, row, resid, col0, r);
+    lane_unpack(r, lg.dtype, resid, x, qv);
+  } else {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) s += static_cast<double>(w[i]);
+    for (int i = 0; i < 8; ++i) {
+      const bool in = col0 + i < lg.vocab;
+      x[i] = in ? load_logit(lg, row, col0 + i) : -kInfF;
+      qv[i] = (resid && in) ? __ldg(q + row * ldq + col0 + i) : 0.0f;
+    }
+  }
+  weights_from_values(x, qv, rs, inv_z, mode, excl, n_excl, col0, w);
+}
+
+// A lane's weight sum: fp32, left to right.  Pass B walks the same additions.
+__device__ __forceinline__ float lane_sum(const float (&w)[8]) {
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) s = __fadd_rn(s, w[i]);
   return s;
 }
 
 __device__ __forceinline__ float inverse_z(const RowStat& rs) { return static_cast<float>(1.0 / rs.Z); }
 
-// Block-wide exclusive scan (lane order, then warp order).  smem: NW + 1.
-template <typename Tv, int BS>
+// Barrier over the first BS threads: the named barrier when a producer warp
+// beyond them must not take part, else the whole block.
+template <int BS, bool NAMED>
+__device__ __forceinline__ void group_sync() {
+  if (NAMED) {
+    named_sync(BS);
+  } else {
+    __syncthreads();
+  }
+}
+
+// Exclusive scan over the first BS threads (lane order, then warp order).  smem: NW + 1.
+template <typename Tv, int BS, bool NAMED = false>
 __device__ __forceinline__ Tv block_exclusive_scan(Tv v, Tv* smem, Tv* total) {
   constexpr int NW = BS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -123,7 +165,7 @@ __device__ __forceinline__ Tv block_exclusive_scan(Tv v, Tv* smem, Tv* total) {
     if (lane >= off) incl += t;
   }
   if (lane == 31) smem[warp] = incl;
-  __syncthreads();
+  group_sync<BS, NAMED>();
   if (warp == 0) {
     const Tv w = lane < NW ? smem[lane] : Tv(0);
     Tv wi = w;
@@ -135,17 +177,19 @@ __device__ __forceinline__ Tv block_exclusive_scan(Tv v, Tv* smem, Tv* total) {
     if (lane < NW) smem[lane] = wi - w;
     if (lane == NW - 1) smem[NW] = wi;
   }
-  __syncthreads();
+  group_sync<BS, NAMED>();
   const Tv res = smem[warp] + (incl - v);
   *total = smem[NW];
-  __syncthreads();
+  group_sync<BS, NAMED>();
   return res;
 }
 
-// Commit bookkeeping for the whole batch by one CTA: commit_cu = exclusive
+// Commit bookkeeping for the whole batch by the first kCommitThreads threads
+// of a block: commit_cu = exclusive
 // scan of num_out; for committed row k of request b, its KV slot and its
-// destination position seq_lens[b] + k.
-__device__ void commit_block(const OutView& out, const CommitParams& cp) {
+// destination position seq_lens[b] + k.  Needs only the acceptance results.
+template <bool NAMED>
+__device__ __forceinline__ void commit_block_t(const OutView& out, const CommitParams& cp) {
   __shared__ int64_t s_scan[kCommitThreads / 32 + 1];
   const int B = cp.batch, ML = cp.max_len;
   const int per = (B + kCommitThreads - 1) / kCommitThreads;
@@ -153,172 +197,404 @@ __device__ void commit_block(const OutView& out, const CommitParams& cp) {
   int64_t local = 0;
   for (int b = ba; b < bb; ++b) local += out.num_out[b];
   int64_t total;
-  int64_t run = block_exclusive_scan<int64_t, kCommitThreads>(local, s_scan, &total);
+  int64_t run = block_exclusive_scan<int64_t, kCommitThreads, NAMED>(local, s_scan, &total);
   for (int b = ba; b < bb; ++b) {
     out.commit_cu[b] = static_cast<int32_t>(run);
+    run += out.num_out[b];
+  }
+  if (threadIdx.x == kCommitThreads - 1) {
+    out.commit_cu[B] = static_cast<int32_t>(total);
+    if (cp.err) *cp.err = 0u;
+  }
+  group_sync<kCommitThreads, NAMED>();  // commit_cu visible to the whole group
+  if (!out.commit_src_slot && !out.commit_dst_pos) return;
+  // one (request, k) entry per thread and step; all loads of a step are independent
+  for (int64_t e = threadIdx.x; e < static_cast<int64_t>(B) * ML; e += kCommitThreads) {
+    const int b = static_cast<int>(e / ML), k = static_cast<int>(e % ML);
     const int n = out.num_out[b];
-    for (int k = 0; k < n; ++k) {
-      const int64_t idx = run + k;
-      if (out.commit_src_slot && cp.row_slots) {
-        const int32_t row = out.accept_rows[static_cast<int64_t>(b) * ML + k];
-        out.commit_src_slot[idx] = cp.row_slots[row];
+    const int32_t row = out.accept_rows[e];
+    const int64_t base = out.commit_cu[b];
+    if (k >= n) continue;
+    if (out.commit_src_slot && cp.row_slots) out.commit_src_slot[base + k] = cp.row_slots[row];
+    if (out.commit_dst_pos && cp.seq_lens) out.commit_dst_pos[base + k] = cp.seq_lens[b] + k;
+  }
+}
+
+__device__ __forceinline__ void commit_block(const OutView& out, const CommitParams& cp) { commit_block_t<false>(out, cp); }
+__device__ __forceinline__ void commit_block_named(const OutView& out, const CommitParams& cp) {
+  commit_block_t<true>(out, cp);
+}
+
+// Weight sums of tiles [ta, tb) of one request's sampled row, U consecutive
+// tiles in flight per warp; lane 0 stores each tile's sum.  Specialised on
+// the logits type and on whether q is read, so no unused loads stay live.
+template <int DT, bool RESID>
+__device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
+                                                 const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
+                                                 int32_t n_excl, int ta, int tb, double* ts) {
+  constexpr int U = 4;
+  const int lane = threadIdx.x & 31;
+  const int full_tiles = lg.vocab / kTile;
+  for (int t0 = ta; t0 < tb; t0 += U) {
+    float ls[U];
+    if (t0 + U <= tb && t0 + U <= full_tiles) {  // all loads first, then the arithmetic
+      uint4 l0[U], l1[U], q0[U], q1[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t col0 = static_cast<int64_t>(t0 + u) * kTile + lane * 8;
+        if (DT == SV_BF16) {
+          l0[u] = ld_stream16(static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 2);
+        } else {
+          const char* base = static_cast<const char*>(lg.base) + (row * lg.ld + col0) * 4;
+          l0[u] = ld_stream16(base);
+          l1[u] = ld_stream16(base + 16);
+        }
+        if (RESID) {
+          const char* qb = reinterpret_cast<const char*>(q + row * ldq + col0);
+          q0[u] = ld_stream16(qb);
+          q1[u] = ld_stream16(qb + 16);
+        }
       }
-      if (out.commit_dst_pos && cp.seq_lens) out.commit_dst_pos[idx] = cp.seq_lens[b] + k;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        LaneRaw r;
+        r.l0 = l0[u];
+        if (DT != SV_BF16) r.l1 = l1[u];
+        if (RESID) {
+          r.q0 = q0[u];
+          r.q1 = q1[u];
+        }
+        float x[8], qv[8], w[8];
+        lane_unpack(r, DT, RESID, x, qv);
+        weights_from_values(x, qv, rs, inv_z, mode, excl, n_excl, static_cast<int64_t>(t0 + u) * kTile + lane * 8,
+                            w);
+        ls[u] = lane_sum(w);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float w[8];
+        if (t0 + u < tb) {
+          lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, static_cast<int64_t>(t0 + u) * kTile + lane * 8,
+                       w);
+          ls[u] = lane_sum(w);
+        } else {
+          ls[u] = 0.0f;
+        }
+      }
     }
-    run += n;
-  }
-  if (threadIdx.x == kCommitThreads - 1) out.commit_cu[B] = static_cast<int32_t>(total);
-}
-
-// Pass A: weight sums of every tile of the sampled rows.  grid = (chunks, batch).
-__global__ void __launch_bounds__(kSampleThreads) k_sample_tiles(LogitsView lg, const float* q, int64_t ldq, Ws ws,
-                                                                 int32_t excl_stride) {
-  const int b = blockIdx.y;
-  const ReqState rq = ws.state[b];
-  if (!sampling_mode(rq.mode)) return;
-  const int64_t row = rq.sample_row;
-  const RowStat rs = ws.rowstat[row];
-  const float inv_z = inverse_z(rs);
-  const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
-  const int T = ws.ntiles;
-  const int nchunk = gridDim.x;
-  const int t0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * T / nchunk);
-  const int t1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * T / nchunk);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int tile = t0 + warp; tile < t1; tile += kSampleWarps) {
-    float w[8];
-    lane_weights(lg, q, ldq, row, rs, inv_z, rq.mode, excl, rq.n_excl, static_cast<int64_t>(tile) * kTile + lane * 8,
-                 w);
-    const double s = warp_sum_xor(lane_sum(w));
-    if (lane == 0) ws.tsum[static_cast<int64_t>(b) * T + tile] = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {  // U butterflies, interleaved
+#pragma unroll
+      for (int u = 0; u < U; ++u) ls[u] += __shfl_xor_sync(0xffffffffu, ls[u], off);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (t0 + u < tb) ts[t0 + u] = static_cast<double>(ls[u]);
+    }
   }
 }
 
-// Pass B + commit.  grid = batch.
-__global__ void __launch_bounds__(kSampleThreads) k_sample_finish(LogitsView lg, const float* q, int64_t ldq,
-                                                                  const float* u_final, OutView out,
-                                                                  CommitParams cp, Ws ws, int32_t excl_stride) {
+__device__ __forceinline__ void warp_tile_sums(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
+                                               const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
+                                               int32_t n_excl, int ta, int tb, double* ts) {
+  const bool resid = mode == kModeResidual;
+  if (lg.dtype == SV_BF16) {
+    if (resid) {
+      warp_tile_sums_t<SV_BF16, true>(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, ta, tb, ts);
+    } else {
+      warp_tile_sums_t<SV_BF16, false>(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, ta, tb, ts);
+    }
+  } else {
+    if (resid) {
+      warp_tile_sums_t<SV_F32, true>(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, ta, tb, ts);
+    } else {
+      warp_tile_sums_t<SV_F32, false>(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, ta, tb, ts);
+    }
+  }
+}
+
+// The draw of one request by one CTA, once all its tile sums exist: scan the
+// tile sums, pick the tile holding t = u_final * S, then one warp re-forms
+// that tile's weights (same arithmetic as the sums) and walks to the entry.
+template <bool NAMED>
+__device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
+                                           const OutView& out, const CommitParams& cp, const Ws& ws,
+                                           int32_t excl_stride, int b, const ReqState& rq) {
   __shared__ double s_scan[kSampleWarps + 1];
   __shared__ int s_tile;
   __shared__ int s_last_nz;
   __shared__ double s_pre;
-  __shared__ int s_last;
-  const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const ReqState rq = ws.state[b];
-  if (sampling_mode(rq.mode)) {
+  const int T = ws.ntiles;
+  const int64_t row = rq.sample_row;
+  const RowStat rs = ws.rowstat[row];
+  const float inv_z = inverse_z(rs);
+  const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
+  double* ts = ws.tsum + static_cast<int64_t>(b) * T;
+  int32_t mode = rq.mode;
+  uint32_t st_add = 0u;
+  const int per = (T + kSampleThreads - 1) / kSampleThreads;
+  const int ta = min(T, tid * per), tb = min(T, ta + per);
+
+  double loc = 0.0;
+  for (int j = ta; j < tb; ++j) loc += __ldcg(ts + j);
+  double total;
+  double pre = block_exclusive_scan<double, kSampleThreads, NAMED>(loc, s_scan, &total);
+  if (!(total > 0.0)) {  // residual (or what is left of p) is empty: draw from p instead
+    mode = kModeP;
+    st_add = kStResidualEmpty;
+    warp_tile_sums(lg, q, ldq, row, rs, inv_z, mode, excl, 0, warp * ((T + kSampleWarps - 1) / kSampleWarps),
+                   min(T, (warp + 1) * ((T + kSampleWarps - 1) / kSampleWarps)), ts);
+    __threadfence_block();
+    group_sync<kSampleThreads, NAMED>();
+    loc = 0.0;
+    for (int j = ta; j < tb; ++j) loc += __ldcg(ts + j);
+    pre = block_exclusive_scan<double, kSampleThreads, NAMED>(loc, s_scan, &total);
+  }
+  const double t = static_cast<double>(u_final[b]) * total;
+  if (tid == 0) {
+    s_tile = INT_MAX;
+    s_last_nz = -1;
+  }
+  group_sync<kSampleThreads, NAMED>();
+  int my_tile = INT_MAX, my_nz = -1;
+  double my_pre = 0.0, run = pre;
+  for (int j = ta; j < tb; ++j) {
+    const double wj = __ldcg(ts + j);
+    if (wj > 0.0) {
+      my_nz = j;
+      if (my_tile == INT_MAX && run <= t && t < run + wj) {
+        my_tile = j;
+        my_pre = run;
+      }
+    }
+    run += wj;
+  }
+  if (my_tile != INT_MAX) atomicMin(&s_tile, my_tile);
+  if (my_nz >= 0) atomicMax(&s_last_nz, my_nz);
+  group_sync<kSampleThreads, NAMED>();
+  if (my_tile != INT_MAX && my_tile == s_tile) s_pre = my_pre;
+  group_sync<kSampleThreads, NAMED>();
+  if (warp != 0) return;
+
+  const bool located = s_tile != INT_MAX;
+  int v = -1;
+  if (located || s_last_nz >= 0) {
+    const int tile = located ? s_tile : s_last_nz;
+    const double tpre = located ? s_pre : 0.0;
+    const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
+    float w[8];
+    lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, mode == kModePExcl ? rq.n_excl : 0, col0, w);
+    const double ls = static_cast<double>(lane_sum(w));
+    const double li = warp_inclusive_scan(ls);
+    const double lo = tpre + (li - ls), hi = tpre + li;
+    const unsigned hit = __ballot_sync(0xffffffffu, located && ls > 0.0 && lo <= t && t < hi);
+    if (hit) {
+      const int f = __ffs(hit) - 1;
+      int cand = -1;
+      if (lane == f) {
+        float cum = 0.0f;  // the same fp32 additions as lane_sum
+        for (int i = 0; i < 8; ++i) {
+          cum = __fadd_rn(cum, w[i]);
+          if (cand < 0 && lo + static_cast<double>(cum) > t) cand = i;
+        }
+        if (cand < 0)
+          for (int i = 7; i >= 0; --i)
+            if (cand < 0 && w[i] > 0.0f) cand = i;
+      }
+      cand = __shfl_sync(0xffffffffu, cand, f);
+      v = static_cast<int>(static_cast<int64_t>(tile) * kTile + f * 8 + cand);
+    } else {  // rounding left t outside every lane: last positive entry of the tile
+      const unsigned nz = __ballot_sync(0xffffffffu, ls > 0.0);
+      const int f = nz ? 31 - __clz(nz) : 0;
+      int cand = -1;
+      if (lane == f)
+        for (int i = 7; i >= 0; --i)
+          if (cand < 0 && w[i] > 0.0f) cand = i;
+      cand = __shfl_sync(0xffffffffu, cand, f);
+      v = cand < 0 ? -1 : static_cast<int>(static_cast<int64_t>(tile) * kTile + f * 8 + cand);
+    }
+  } else {
+    st_add |= kStNonFinite;  // no positive weight at all (not reachable for a usable row)
+  }
+  if (lane == 0) {
+    out.bonus[b] = v;
+    out.out_tokens[static_cast<int64_t>(b) * cp.max_len + rq.r] = v;
+    if (st_add) out.dev_status[b] = rq.status | st_add;
+  }
+}
+
+// Final token and commit.  The batch's (request, tile) space is split into
+// equal contiguous ranges, one per block (one resident wave).  In each block a
+// producer warp streams the sampled rows' tiles (logits, and q for a
+// residual) through a ring of shared-memory stages with bulk copies; eight
+// consumer warps sum the weights of every tile.  After its part of a request
+// the block takes a ticket on the request, and the block completing the
+// request draws its token while the producer keeps streaming.  One extra
+// block performs the commit (it needs only the acceptance results).  Every
+// wait is bounded; no block waits on another.
+constexpr int kSampleStages = 3;
+constexpr int kSampleStageBytes = 32 * 1024;
+constexpr int kSampleStageMaxTiles = 32;
+constexpr uint64_t kSampleWaitNs = 1000000000ull;
+constexpr int kSampleBlockThreads = kSampleThreads + 32;  // consumers + one producer warp
+constexpr size_t kSampleSmemBytes = static_cast<size_t>(kSampleStages) * kSampleStageBytes + 256;
+
+struct SampleRing {
+  unsigned long long full[kSampleStages];
+  unsigned long long empty[kSampleStages];
+  int last;
+  int abort;
+};
+
+__device__ __forceinline__ int stage_tiles(int dtype, bool resid) {
+  const int tb = kTile * ((dtype == SV_BF16 ? 2 : 4) + (resid ? 4 : 0));
+  const int n = kSampleStageBytes / tb;
+  return n < kSampleStageMaxTiles ? n : kSampleStageMaxTiles;
+}
+
+__global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg, const float* q, int64_t ldq,
+                                                                   const float* u_final, OutView out,
+                                                                   CommitParams cp, Ws ws, int32_t excl_stride,
+                                                                   int32_t nblocks) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ SampleRing ring;
+  if (static_cast<int>(blockIdx.x) == nblocks) {  // the commit block
+    if (threadIdx.x < kCommitThreads) commit_block_named(out, cp);
+    return;
+  }
+  unsigned char* stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                           ~uintptr_t(127));
+  const int T = ws.ntiles;
+  const int full_tiles = lg.vocab / kTile;
+  const int es = lg.dtype == SV_BF16 ? 2 : 4;
+  const int64_t total = static_cast<int64_t>(cp.batch) * T;
+  const int64_t t_begin = blockIdx.x * total / nblocks, t_end = (blockIdx.x + 1) * total / nblocks;
+  if (t_begin >= t_end) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSampleStages; ++i) {
+      mbar_init(smem_addr(&ring.full[i]), 1);
+      mbar_init(smem_addr(&ring.empty[i]), kSampleWarps);
+    }
+    ring.abort = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == kSampleWarps) {  // ------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      for (int64_t b = t_begin / T; b * T < t_end && !ring.abort; ++b) {
+        const int ta = static_cast<int>((t_begin > b * T ? t_begin : b * T) - b * T);
+        const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
+        const ReqState rq = ws.state[b];
+        if (!sampling_mode(rq.mode)) continue;
+        const bool resid = rq.mode == kModeResidual;
+        const int per = stage_tiles(lg.dtype, resid);
+        const int tc = min(tb, full_tiles);
+        const int64_t row = rq.sample_row;
+        for (int c0 = ta; c0 < tc; c0 += per, ++g) {
+          const int n = min(per, tc - c0);
+          const int st = g % kSampleStages;
+          if (!mbar_wait_bounded(smem_addr(&ring.empty[st]), ((g / kSampleStages) & 1u) ^ 1u, &ring.abort,
+                                 kSampleWaitNs)) {
+            ring.abort = 1;
+            atomicOr(ws.err, 1u);
+            break;
+          }
+          const uint32_t lb = static_cast<uint32_t>(n) * kTile * es;
+          const uint32_t qb = resid ? static_cast<uint32_t>(n) * kTile * 4 : 0u;
+          unsigned char* dst = stages + static_cast<size_t>(st) * kSampleStageBytes;
+          mbar_arrive_expect_tx(smem_addr(&ring.full[st]), lb + qb);
+          bulk_copy_g2s(smem_addr(dst),
+                        static_cast<const char*>(lg.base) + (row * lg.ld + static_cast<int64_t>(c0) * kTile) * es, lb,
+                        smem_addr(&ring.full[st]));
+          if (qb)
+            bulk_copy_g2s(smem_addr(dst + lb), q + row * ldq + static_cast<int64_t>(c0) * kTile, qb,
+                          smem_addr(&ring.full[st]));
+        }
+      }
+      for (int i = 0; i < kSampleStages && g > 0; ++i) {  // drain before the block may exit
+        --g;
+        volatile int never = 0;
+        mbar_wait_bounded(smem_addr(&ring.full[g % kSampleStages]), (g / kSampleStages) & 1u, &never,
+                          kSampleWaitNs);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------------- consumers
+  uint32_t g = 0;
+  for (int64_t b = t_begin / T; b * T < t_end; ++b) {
+    const int ta = static_cast<int>((t_begin > b * T ? t_begin : b * T) - b * T);
+    const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
+    const ReqState rq = ws.state[b];
+    if (!sampling_mode(rq.mode)) continue;
+    const bool resid = rq.mode == kModeResidual;
+    const int per = stage_tiles(lg.dtype, resid);
+    const int tc = min(tb, full_tiles);
     const int64_t row = rq.sample_row;
     const RowStat rs = ws.rowstat[row];
     const float inv_z = inverse_z(rs);
     const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
-    const int T = ws.ntiles;
     double* ts = ws.tsum + static_cast<int64_t>(b) * T;
-    int32_t mode = rq.mode;
-    uint32_t st_add = 0u;
-    const int per = (T + kSampleThreads - 1) / kSampleThreads;
-    const int ta = min(T, tid * per), tb = min(T, ta + per);
-
-    double loc = 0.0;
-    for (int j = ta; j < tb; ++j) loc += ts[j];
-    double total;
-    double pre = block_exclusive_scan<double, kSampleThreads>(loc, s_scan, &total);
-    if (!(total > 0.0)) {  // residual (or what is left of p) is empty: draw from p instead
-      mode = kModeP;
-      st_add = kStResidualEmpty;
-      for (int tile = warp; tile < T; tile += kSampleWarps) {
-        float w[8];
-        lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, 0, static_cast<int64_t>(tile) * kTile + lane * 8, w);
-        const double s = warp_sum_xor(lane_sum(w));
-        if (lane == 0) ts[tile] = s;
-      }
-      __syncthreads();
-      loc = 0.0;
-      for (int j = ta; j < tb; ++j) loc += ts[j];
-      pre = block_exclusive_scan<double, kSampleThreads>(loc, s_scan, &total);
-    }
-    const double t = static_cast<double>(u_final[b]) * total;
-    if (tid == 0) {
-      s_tile = INT_MAX;
-      s_last_nz = -1;
-    }
-    __syncthreads();
-    int my_tile = INT_MAX, my_nz = -1;
-    double my_pre = 0.0, run = pre;
-    for (int j = ta; j < tb; ++j) {
-      const double wj = ts[j];
-      if (wj > 0.0) {
-        my_nz = j;
-        if (my_tile == INT_MAX && run <= t && t < run + wj) {
-          my_tile = j;
-          my_pre = run;
-        }
-      }
-      run += wj;
-    }
-    if (my_tile != INT_MAX) atomicMin(&s_tile, my_tile);
-    if (my_nz >= 0) atomicMax(&s_last_nz, my_nz);
-    __syncthreads();
-    if (my_tile != INT_MAX && my_tile == s_tile) s_pre = my_pre;
-    __syncthreads();
-
-    if (warp == 0 && (s_tile != INT_MAX || s_last_nz >= 0)) {
-      const bool located = s_tile != INT_MAX;
-      const int tile = located ? s_tile : s_last_nz;
-      const double tpre = located ? s_pre : 0.0;
-      const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
-      float w[8];
-      lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, mode == kModePExcl ? rq.n_excl : 0, col0, w);
-      const double ls = lane_sum(w);
-      const double incl = warp_inclusive_scan(ls);
-      const double lo = tpre + (incl - ls), hi = tpre + incl;
-      int v = -1;
-      const unsigned hit = __ballot_sync(0xffffffffu, located && ls > 0.0 && lo <= t && t < hi);
-      if (hit) {
-        const int f = __ffs(hit) - 1;
-        int cand = -1;
-        if (lane == f) {
-          double cum = lo;
-          for (int i = 0; i < 8; ++i) {
-            cum += static_cast<double>(w[i]);
-            if (cand < 0 && cum > t) cand = i;
+    for (int c0 = ta; c0 < tc; c0 += per, ++g) {
+      const int n = min(per, tc - c0);
+      const int st = g % kSampleStages;
+      const unsigned char* src = stages + static_cast<size_t>(st) * kSampleStageBytes;
+      const uint32_t lb = static_cast<uint32_t>(n) * kTile * es;
+      if (!mbar_wait_bounded(smem_addr(&ring.full[st]), (g / kSampleStages) & 1u, &ring.abort, kSampleWaitNs)) {
+        ring.abort = 1;
+        atomicOr(ws.err, 1u);
+      } else {
+        for (int i = warp; i < n; i += kSampleWarps) {
+          const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
+          LaneRaw r;
+          r.l0 = lds16(smem_addr(src) + off * es);
+          if (es == 4) r.l1 = lds16(smem_addr(src) + off * es + 16);
+          if (resid) {
+            r.q0 = lds16(smem_addr(src + lb) + off * 4);
+            r.q1 = lds16(smem_addr(src + lb) + off * 4 + 16);
           }
-          if (cand < 0)
-            for (int i = 7; i >= 0; --i)
-              if (cand < 0 && w[i] > 0.0f) cand = i;
+          float x[8], qv[8], w[8];
+          lane_unpack(r, lg.dtype, resid, x, qv);
+          weights_from_values(x, qv, rs, inv_z, rq.mode, excl, rq.n_excl,
+                              static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+          float ls = lane_sum(w);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+          if (lane == 0) ts[c0 + i] = static_cast<double>(ls);
         }
-        cand = __shfl_sync(0xffffffffu, cand, f);
-        v = static_cast<int>(static_cast<int64_t>(tile) * kTile + f * 8 + cand);
-      } else {  // rounding left t outside every lane: last positive entry of the tile
-        const unsigned nz = __ballot_sync(0xffffffffu, ls > 0.0);
-        const int f = nz ? 31 - __clz(nz) : 0;
-        int cand = -1;
-        if (lane == f)
-          for (int i = 7; i >= 0; --i)
-            if (cand < 0 && w[i] > 0.0f) cand = i;
-        cand = __shfl_sync(0xffffffffu, cand, f);
-        v = cand < 0 ? -1 : static_cast<int>(static_cast<int64_t>(tile) * kTile + f * 8 + cand);
       }
-      if (lane == 0) {
-        out.bonus[b] = v;
-        out.out_tokens[static_cast<int64_t>(b) * cp.max_len + rq.r] = v;
-        if (st_add) out.dev_status[b] = rq.status | st_add;
-      }
-    } else if (warp == 0 && lane == 0) {  // no positive weight at all (not reachable for a usable row)
-      out.bonus[b] = -1;
-      out.dev_status[b] = rq.status | st_add | kStNonFinite;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&ring.empty[st]));
     }
-  }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned ticket = atomicAdd(ws.done_cnt, 1u);
-    s_last = (ticket == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    commit_block(out, cp);
-    if (tid == 0) *ws.done_cnt = 0u;
+    for (int tile = max(tc, ta) + warp; tile < tb; tile += kSampleWarps) {  // the ragged last tile
+      float w[8];
+      lane_weights(lg, q, ldq, row, rs, inv_z, rq.mode, excl, rq.n_excl, static_cast<int64_t>(tile) * kTile + lane * 8,
+                   w);
+      float ls = lane_sum(w);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      if (lane == 0) ts[tile] = static_cast<double>(ls);
+    }
+    named_sync(kSampleThreads);
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const unsigned add = static_cast<unsigned>(tb - ta);
+      ring.last = (atomicAdd(&ws.chunk_cnt[b], add) + add == static_cast<unsigned>(T));
+    }
+    named_sync(kSampleThreads);
+    if (ring.last) {
+      __threadfence();
+      block_draw<true>(lg, q, ldq, u_final, out, cp, ws, excl_stride, static_cast<int>(b), rq);
+      if (threadIdx.x == 0) ws.chunk_cnt[b] = 0u;  // leave the counter clean for the next call
+      named_sync(kSampleThreads);
+    }
   }
 }
 
@@ -326,17 +602,21 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitPa
 
 }  // namespace
 
+cudaError_t sample_smem_setup() {
+  return cudaFuncSetAttribute(k_sample, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSampleSmemBytes));
+}
+
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
                                      const DeviceInfo& dev, cudaStream_t stream) {
-  const int T = ws.ntiles;
-  int nchunk = (4 * dev.sms + cp.batch - 1) / cp.batch;
-  if (nchunk > T) nchunk = T;
-  if (nchunk < 1) nchunk = 1;
-  k_sample_tiles<<<dim3(nchunk, cp.batch), kSampleThreads, 0, stream>>>(lg, q, ldq, ws, cp.max_len);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_sample_finish<<<cp.batch, kSampleThreads, 0, stream>>>(lg, q, ldq, u_final, out, cp, ws, cp.max_len);
+  // one resident wave (two blocks per SM), at least ~16 tiles per block
+  const int64_t tiles = static_cast<int64_t>(cp.batch) * ws.ntiles;
+  int64_t nblocks = static_cast<int64_t>(dev.sms) * 2;
+  if (nblocks > (tiles + 15) / 16) nblocks = (tiles + 15) / 16;
+  if (nblocks < 1) nblocks = 1;
+  k_sample<<<static_cast<unsigned>(nblocks + 1), kSampleBlockThreads, kSampleSmemBytes, stream>>>(
+      lg, q, ldq, u_final, out, cp, ws, cp.max_len, static_cast<int32_t>(nblocks));
   return cudaGetLastError();
 }
 

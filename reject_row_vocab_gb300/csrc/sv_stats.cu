@@ -11,7 +11,14 @@
 // range boundaries is finished by the last CTA that touches it: each CTA
 // publishes its partial (m, s, argmax) for the cut rows, takes a ticket on the
 // row's counter, and the CTA drawing the final ticket merges the partials in
-// CTA order (deterministic) and resets the counter.  No CTA ever waits.
+// CTA order (deterministic) and resets the counter.  No CTA waits on another.
+//
+// Data movement: one producer warp streams the CTA's range into a ring of
+// shared-memory stages with bulk copies (the TMA engine, completion counted on
+// an mbarrier per stage); eight consumer warps fold each stage and release it.
+// Bytes in flight per SM are set by the ring, not by registers.  Every wait is
+// bounded (one second); a timeout raises the workspace error word, which the
+// acceptance kernels report as SV_DEV_TIMEOUT.
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -20,7 +27,35 @@
 namespace sv {
 namespace {
 
-constexpr int kStatsThreads = 256;
+constexpr int kConsumers = 256;                      // eight consumer warps
+constexpr int kProducerWarp = kConsumers / 32;       // warp 8 streams the stages
+constexpr int kFinalizerWarp = kProducerWarp + 1;    // warp 9 finishes each row
+constexpr int kStatsThreads = kConsumers + 64;
+constexpr int kChunkVecs = 1024;                     // 16 KB per stage
+constexpr int kStages = 4;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr int kRowsCached = 64;  // per-row log2(e)/T precomputed for the first rows of a range
+
+// One consumer thread's statistics for one row segment, handed to the finalizer.
+struct SegSlot {
+  float m;
+  float s;        // sum of 2^((l - m) k)
+  int32_t vidx;   // vector holding the first occurrence of m (to resolve), or -1
+  int32_t idx;    // resolved index when vidx < 0
+  uint32_t flags;
+};
+
+struct StatsSmem {
+  uint4 buf[kStages][kChunkVecs];
+  SegSlot seg[2][kConsumers];
+  unsigned long long full[kStages];
+  unsigned long long empty[kStages];
+  unsigned long long seg_full[2];
+  unsigned long long seg_empty[2];
+  float kc[kRowsCached];
+  int abort;
+};
+constexpr size_t kStatsSmemBytes = sizeof(StatsSmem) + 128;  // + alignment slack
 
 template <int DT>
 struct VecTraits;
@@ -28,24 +63,40 @@ template <>
 struct VecTraits<SV_BF16> {
   static constexpr int E = 8;   // elements per 16-byte vector
   static constexpr int ES = 2;  // element bytes
-  static constexpr int U = 4;   // vectors in flight per thread
 };
 template <>
 struct VecTraits<SV_F32> {
   static constexpr int E = 4;
   static constexpr int ES = 4;
-  static constexpr int U = 4;
 };
 
-// Per-thread running statistics.  The scaled sum uses Kahan compensation so
-// its error does not grow with the number of vectors a thread visits.
+// Per-thread running statistics: maximum m, the vector where m was last
+// raised (its element index is resolved once, at the end of the range), the
+// resolved argmax, flags, and a packed fp32 accumulator of 2^((l - r) k)
+// against a reference r that trails m: r only moves when m outgrows it by
+// more than kRefSlack (in log2 units), so most vectors need no rescale.
 struct ThreadAcc {
   float m;
-  float s;
-  float c;
-  int32_t idx;
+  int32_t vidx;  // vector (within the row) holding the first occurrence of m, -1 if none yet
+  int32_t idx;   // resolved argmax (tail handling and after resolution)
   uint32_t flags;
+  float r;       // exponent reference, starts at -FLT_MAX (finite: no inf - inf)
+  float2 s;
 };
+
+constexpr float kRefSlack = 16.0f;  // terms stay <= 2^16 between reference moves
+constexpr float kMinFinite = -3.402823466e38f;
+
+__device__ __forceinline__ ThreadAcc acc_init() {
+  return ThreadAcc{-kInfF, -1, -1, 0u, kMinFinite, make_float2(0.0f, 0.0f)};
+}
+
+// The accumulated sum expressed against the maximum m (for merging).
+__device__ __forceinline__ float acc_sum_at_max(const ThreadAcc& a, float k) {
+  const float s = a.s.x + a.s.y;
+  if (s == 0.0f || a.r == a.m) return s;
+  return s * exp2f((a.r - a.m) * k);
+}
 
 template <int DT>
 __device__ __forceinline__ void unpack(const uint4& raw, float (&x)[VecTraits<DT>::E]) {
@@ -79,89 +130,122 @@ __device__ __forceinline__ float raw_max_nan(const uint4& raw) {
   }
 }
 
-// Fold E consecutive logits starting at column col0 into the accumulator.
-template <int E, bool EXP>
-__device__ __forceinline__ void consume(ThreadAcc& a, float (&x)[E], float vmax_nan, int64_t col0, float k) {
-  float vmax = vmax_nan;
-  if (!(vmax_nan < kInfF)) {  // NaN or +inf present: exclude those entries
-    vmax = -kInfF;
+// Sum of 2^((x - m) k) over E elements, as a packed pair (fixed order).
+template <int E>
+__device__ __forceinline__ float2 exp_sum(const float (&x)[E], float m, float k) {
+  const float2 nm = make_float2(-m, -m), kk = make_float2(k, k);
+  float2 e[E / 2];
 #pragma unroll
-    for (int i = 0; i < E; ++i) {
-      if (!usable_logit(x[i])) {
-        x[i] = -kInfF;
-        a.flags |= kStNonFinite;
-      }
-      vmax = fmaxf(vmax, x[i]);
-    }
+  for (int i = 0; i < E / 2; ++i) {
+    const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), nm), kk);
+    e[i] = make_float2(ex2_fast(t.x), ex2_fast(t.y));
   }
-  if (vmax > a.m) {  // new running maximum (rare after the first vectors)
-    if (EXP && a.m > -kInfF) {
-      const float f = exp2f((a.m - vmax) * k);
-      a.s *= f;
-      a.c *= f;
-    }
-    a.m = vmax;
-    int j = E - 1;
-#pragma unroll
-    for (int i = E - 1; i >= 0; --i)
-      if (x[i] == vmax) j = i;
-    a.idx = static_cast<int32_t>(col0 + j);
-  }
-  if (EXP && a.m > -kInfF) {
-    float e[E];
-#pragma unroll
-    for (int i = 0; i < E; ++i) e[i] = ex2_fast((x[i] - a.m) * k);
-    float vs;
-    if constexpr (E == 8) {
-      vs = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-    } else {
-      vs = (e[0] + e[1]) + (e[2] + e[3]);
-    }
-    const float y = vs - a.c;
-    const float t = a.s + y;
-    a.c = (t - a.s) - y;
-    a.s = t;
+  if constexpr (E == 8) {
+    return __fadd2_rn(__fadd2_rn(e[0], e[1]), __fadd2_rn(e[2], e[3]));
+  } else {
+    return __fadd2_rn(e[0], e[1]);
   }
 }
 
-// Scan vectors [v0, v1) of one row (vector index within the row).
-template <int DT, bool EXP>
-__device__ __forceinline__ void scan_row_range(const LogitsView& lg, int64_t row, int64_t v0, int64_t v1, float k,
-                                               ThreadAcc& a) {
-  using VT = VecTraits<DT>;
-  constexpr int E = VT::E, U = VT::U, BS = kStatsThreads;
-  const char* rowp = static_cast<const char*>(lg.base) + row * lg.ld * VT::ES;
-  const int64_t nfull = lg.vocab / E;  // vectors entirely inside the row
-  const int64_t vend = v1 < nfull ? v1 : nfull;
-  int64_t v = v0 + threadIdx.x;
-  for (; v + (U - 1) * BS < vend; v += U * BS) {
-    uint4 raw[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) raw[u] = ld_stream16(rowp + (v + u * BS) * 16);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float x[E];
-      unpack<DT>(raw[u], x);
-      consume<E, EXP>(a, x, raw_max_nan<DT>(raw[u]), (v + u * BS) * E, k);
-    }
-  }
-  for (; v < v1; v += BS) {
-    float x[E];
-    float vmax;
-    if (v < nfull) {
-      const uint4 raw = ld_stream16(rowp + v * 16);
-      unpack<DT>(raw, x);
-      vmax = raw_max_nan<DT>(raw);
-    } else {  // the row's ragged tail: element loads, padding is -inf
-      vmax = -kInfF;
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        const int64_t col = v * E + i;
-        x[i] = col < lg.vocab ? load_logit(lg, row, col) : -kInfF;
-        vmax = fmax_nan(vmax, x[i]);
+// Fold E logits one at a time, NaN and +inf entries read as -inf (the caller
+// flags them).  immediate: record the argmax index itself, else the vector.
+template <int E, bool EXP>
+__device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E], int32_t vec, float k,
+                                              bool immediate) {
+  for (int i = 0; i < E; ++i) {
+    const float v = usable_logit(x[i]) ? x[i] : -kInfF;
+    if (v > a.m) {
+      a.m = v;
+      if (immediate) {
+        a.idx = vec * E + i;
+        a.vidx = -1;  // the pending vector no longer holds the maximum
+      } else {
+        a.vidx = vec;
       }
     }
-    consume<E, EXP>(a, x, vmax, v * E, k);
+    if (EXP) {
+      if (v > a.r) {  // exact reference moves here (rare path)
+        const float f = a.r > kMinFinite ? exp2f((a.r - v) * k) : 0.0f;
+        a.s = __fmul2_rn(a.s, make_float2(f, f));
+        a.r = v;
+      }
+      a.s.x += ex2_fast((v - a.r) * k);
+    }
+  }
+}
+
+// Fold one vector.  The common case (clean data, maximum within the slack of
+// the reference) is branch-free.
+template <int DT, bool EXP>
+__device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float slack) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+  unpack<DT>(raw, x);
+  const float vmax = raw_max_nan<DT>(raw);
+  const float bound = EXP ? a.r + slack : kInfF;
+  if (!(vmax < bound)) {  // NaN / +inf present, or the maximum outgrew the reference (rare)
+    if (!(vmax < kInfF)) {
+      a.flags |= kStNonFinite;
+      consume_dirty<E, EXP>(a, x, vec, k, false);
+      return;
+    }
+    if (EXP) {
+      const float f = a.r > kMinFinite ? exp2f((a.r - vmax) * k) : 0.0f;
+      a.s = __fmul2_rn(a.s, make_float2(f, f));
+      a.r = vmax;
+    }
+  }
+  const bool raised = vmax > a.m;
+  a.vidx = raised ? vec : a.vidx;
+  a.m = fmaxf(a.m, vmax);
+  if (EXP) a.s = __fadd2_rn(a.s, exp_sum<E>(x, a.r, k));
+}
+
+// The index of the first entry equal to m in vector vidx of a row.
+template <int DT>
+__device__ __forceinline__ int32_t resolve_index(const char* rowp, int32_t vidx, float m) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+  unpack<DT>(ld_stream16(rowp + static_cast<int64_t>(vidx) * 16), x);
+  int j = E - 1;
+#pragma unroll
+  for (int i = E - 1; i >= 0; --i)
+    if (x[i] == m) j = i;
+  return vidx * E + j;
+}
+
+// The row's ragged tail vector (vocab not a multiple of the vector width), by one thread.
+template <int DT, bool EXP>
+__device__ __forceinline__ void fold_tail(ThreadAcc& a, const LogitsView& lg, int64_t row, int64_t nfull, float k) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int64_t col = nfull * E + i;
+    x[i] = col < lg.vocab ? load_logit(lg, row, col) : -kInfF;
+    if (!usable_logit(x[i])) a.flags |= kStNonFinite;
+  }
+  consume_dirty<E, EXP>(a, x, static_cast<int32_t>(nfull), k, true);
+}
+
+// Fold the first n vectors of a stage (chunk starting at vector c0 of the row).
+template <int DT, bool EXP>
+__device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k,
+                                           float slack) {
+  constexpr int PER = kChunkVecs / kConsumers;  // vectors per consumer thread per full stage
+  const int t = threadIdx.x;
+  if (n == kChunkVecs) {
+    uint4 raw[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) raw[j] = lds16(stage_addr + (t + j * kConsumers) * 16);
+#pragma unroll
+    for (int j = 0; j < PER; ++j) consume<DT, EXP>(a, raw[j], c0 + t + j * kConsumers, k, slack);
+  } else {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int vi = t + j * kConsumers;
+      if (vi < n) consume<DT, EXP>(a, lds16(stage_addr + vi * 16), c0 + vi, k, slack);
+    }
   }
 }
 
@@ -197,83 +281,198 @@ __device__ __forceinline__ int64_t cta_of_vector(int64_t v, int64_t G, int64_t N
   return ((v + 1) * G - 1) / NV;
 }
 
+// Segment geometry of one row within a CTA's range.
+struct Seg {
+  int64_t s0, s1, sf;  // vectors [s0, s1) of the row are ours; [s0, sf) are full vectors
+};
+
+__device__ __forceinline__ Seg segment_of(int64_t row, int64_t NVr, int64_t v_begin, int64_t v_end, int64_t nfull) {
+  const int64_t row_v0 = row * NVr;
+  Seg g;
+  g.s0 = (v_begin > row_v0 ? v_begin : row_v0) - row_v0;
+  g.s1 = (v_end < row_v0 + NVr ? v_end : row_v0 + NVr) - row_v0;
+  g.sf = g.s1 < nfull ? g.s1 : nfull;
+  return g;
+}
+
 template <int DT>
-__global__ void __launch_bounds__(kStatsThreads) k_row_stats(LogitsView lg, RowMap map, Ws ws, int64_t NVr,
-                                                             int64_t NV) {
-  __shared__ Part s_red[kStatsThreads / 32];
-  __shared__ float s_k;
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, int64_t NVr,
+                                                                int64_t NV) {
+  using VT = VecTraits<DT>;
+  constexpr int E = VT::E;
+  extern __shared__ unsigned char smem_raw[];
+  StatsSmem& sm = *reinterpret_cast<StatsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int64_t G = gridDim.x, c = blockIdx.x;
   const int64_t v_begin = c * NV / G, v_end = (c + 1) * NV / G;
   if (v_begin >= v_end) return;
   const int64_t r_first = v_begin / NVr, r_last = (v_end - 1) / NVr;
+  const int64_t nfull = lg.vocab / E;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  for (int64_t row = r_first; row <= r_last; ++row) {
-    const int64_t row_v0 = row * NVr;
-    const int64_t s0 = (v_begin > row_v0 ? v_begin : row_v0) - row_v0;
-    const int64_t s1 = (v_end < row_v0 + NVr ? v_end : row_v0 + NVr) - row_v0;
-    if (threadIdx.x == 0) s_k = row_k(map, row);
-    __syncthreads();
-    const float k = s_k;
-
-    ThreadAcc a{-kInfF, 0.0f, 0.0f, -1, 0u};
-    if (k > 0.0f) {
-      scan_row_range<DT, true>(lg, row, s0, s1, k, a);
-    } else {
-      scan_row_range<DT, false>(lg, row, s0, s1, k, a);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&sm.full[s]), 1);
+      mbar_init(smem_addr(&sm.empty[s]), kConsumers / 32);
     }
-    Part p{a.m, static_cast<double>(a.s) - static_cast<double>(a.c), a.idx, a.flags};
-    p = part_block_reduce<kStatsThreads>(p, k, s_red);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_addr(&sm.seg_full[s]), kConsumers);
+      mbar_init(smem_addr(&sm.seg_empty[s]), 1);
+    }
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  // the temperatures of the first rows, fetched once while the first stages load
+  if (threadIdx.x < kRowsCached && r_first + threadIdx.x <= r_last) sm.kc[threadIdx.x] = row_k(map, r_first + threadIdx.x);
+  __syncthreads();
 
-    const int64_t c_lo = cta_of_vector(row_v0, G, NV);
-    const int64_t c_hi = cta_of_vector(row_v0 + NVr - 1, G, NV);
-    if (c_lo == c_hi) {  // the whole row is ours
-      if (threadIdx.x == 0) {
-        RowStat st;
-        st.Z = (k > 0.0f && p.m > -kInfF) ? p.s : 0.0;
-        st.M = p.m;
-        st.argmax = p.idx;
-        st.flags = p.flags;
-        st.k = k;
-        ws.rowstat[row] = st;
+  if (warp == kProducerWarp) {  // ------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t g = 0;
+      for (int64_t row = r_first; row <= r_last && !sm.abort; ++row) {
+        const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
+        const char* rowp = static_cast<const char*>(lg.base) + row * lg.ld * VT::ES;
+        for (int64_t c0 = sg.s0; c0 < sg.sf; c0 += kChunkVecs, ++g) {
+          const int n = static_cast<int>(sg.sf - c0 < kChunkVecs ? sg.sf - c0 : kChunkVecs);
+          const int st = g % kStages;
+          if (!mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
+            sm.abort = 1;
+            atomicOr(ws.err, 1u);
+            break;
+          }
+          mbar_arrive_expect_tx(smem_addr(&sm.full[st]), n * 16);
+          bulk_copy_g2s(smem_addr(&sm.buf[st][0]), rowp + c0 * 16, n * 16, smem_addr(&sm.full[st]));
+        }
       }
-      continue;
-    }
-    if (threadIdx.x == 0) {
-      RowPartial rp;
-      rp.s = p.s;
-      rp.m = p.m;
-      rp.idx = p.idx;
-      rp.flags = p.flags;
-      rp.pad = 0u;
-      ws.partial[2 * c + (row == r_first ? 0 : 1)] = rp;
-      __threadfence();
-      const unsigned ticket = atomicAdd(&ws.row_cnt[row], 1u);
-      s_last = (ticket == static_cast<unsigned>(c_hi - c_lo));
-    }
-    __syncthreads();
-    if (s_last && threadIdx.x < 32) {  // last arriver: merge the row's partials in CTA order
-      __threadfence();
-      const int lane = threadIdx.x;
-      Part acc = part_identity();
-      for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32) {
-        const int64_t first_row_cc = (cc * NV / G) / NVr;
-        const Part q = load_partial_cg(&ws.partial[2 * cc + (row == first_row_cc ? 0 : 1)]);
-        part_merge(acc, q, k);
+      for (int s = 0; s < kStages && g > 0; ++s) {  // drain before the CTA may exit
+        --g;
+        volatile int never = 0;
+        mbar_wait_bounded(smem_addr(&sm.full[g % kStages]), (g / kStages) & 1u, &never, kWaitLimitNs);
       }
-      acc = part_warp_reduce(acc, k);
+    }
+    return;
+  }
+
+  if (warp == kFinalizerWarp) {  // ---------------------------------------- finalizer
+    uint32_t i = 0;
+    for (int64_t row = r_first; row <= r_last; ++row, ++i) {
+      const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
+      const char* rowp = static_cast<const char*>(lg.base) + row * lg.ld * VT::ES;
+      const float k = row - r_first < kRowsCached ? sm.kc[row - r_first] : row_k(map, row);
+      const int slot = i & 1;
+      if (!mbar_wait_bounded(smem_addr(&sm.seg_full[slot]), (i >> 1) & 1u, &sm.abort, kWaitLimitNs)) {
+        sm.abort = 1;
+        atomicOr(ws.err, 1u);
+      }
+      // each lane folds eight consumers' statistics, resolving argmax indices from the row
+      constexpr int PER = kConsumers / 32;
+      SegSlot sl[PER];
+#pragma unroll
+      for (int t = 0; t < PER; ++t) sl[t] = sm.seg[slot][lane * PER + t];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.seg_empty[slot]));  // the slot is free again
+      // Only the consumers holding the segment maximum need their index resolved.
+      float mseg = -kInfF;
+#pragma unroll
+      for (int t = 0; t < PER; ++t) mseg = fmaxf(mseg, sl[t].m);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mseg = fmaxf(mseg, __shfl_xor_sync(0xffffffffu, mseg, off));
+      int32_t idx[PER];
+#pragma unroll
+      for (int t = 0; t < PER; ++t)
+        idx[t] = (sl[t].vidx >= 0 && sl[t].m == mseg) ? resolve_index<DT>(rowp, sl[t].vidx, sl[t].m) : sl[t].idx;
+      Part p = part_identity();
+#pragma unroll
+      for (int t = 0; t < PER; ++t) part_merge(p, Part{sl[t].m, sl[t].s, idx[t], sl[t].flags}, k);
+      p = part_warp_reduce(p, k);
+
+      const int64_t c_lo = cta_of_vector(row * NVr, G, NV);
+      const int64_t c_hi = cta_of_vector(row * NVr + NVr - 1, G, NV);
+      if (c_lo == c_hi) {  // the whole row is ours
+        if (lane == 0) {
+          RowStat st;
+          st.Z = (k > 0.0f && p.m > -kInfF) ? static_cast<double>(p.s) : 0.0;
+          st.M = p.m;
+          st.argmax = p.idx;
+          st.flags = p.flags;
+          st.k = k;
+          ws.rowstat[row] = st;
+        }
+        continue;
+      }
+      int last = 0;
       if (lane == 0) {
-        RowStat st;
-        st.Z = (k > 0.0f && acc.m > -kInfF) ? acc.s : 0.0;
-        st.M = acc.m;
-        st.argmax = acc.idx;
-        st.flags = acc.flags;
-        st.k = k;
-        ws.rowstat[row] = st;
-        ws.row_cnt[row] = 0u;  // leave the counter clean for the next call
+        RowPartial rp;
+        rp.s = static_cast<double>(p.s);
+        rp.m = p.m;
+        rp.idx = p.idx;
+        rp.flags = p.flags;
+        rp.pad = 0u;
+        ws.partial[2 * c + (row == r_first ? 0 : 1)] = rp;
+        __threadfence();
+        const unsigned ticket = atomicAdd(&ws.row_cnt[row], 1u);
+        last = (ticket == static_cast<unsigned>(c_hi - c_lo));
+      }
+      if (__shfl_sync(0xffffffffu, last, 0)) {  // last arriver: merge the row's partials in CTA order
+        __threadfence();
+        PartD acc = partd_identity();
+        for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32) {
+          const int64_t first_row_cc = (cc * NV / G) / NVr;
+          const PartD q = load_partial_cg(&ws.partial[2 * cc + (row == first_row_cc ? 0 : 1)]);
+          partd_merge(acc, q, k);
+        }
+        acc = partd_warp_reduce(acc, k);
+        if (lane == 0) {
+          RowStat st;
+          st.Z = (k > 0.0f && acc.m > -kInfF) ? acc.s : 0.0;
+          st.M = acc.m;
+          st.argmax = acc.idx;
+          st.flags = acc.flags;
+          st.k = k;
+          ws.rowstat[row] = st;
+          ws.row_cnt[row] = 0u;  // leave the counter clean for the next call
+        }
+      }
+      (void)sg;
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  uint32_t g = 0, i = 0;
+  for (int64_t row = r_first; row <= r_last; ++row, ++i) {
+    const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
+    const float k = row - r_first < kRowsCached ? sm.kc[row - r_first] : row_k(map, row);
+    ThreadAcc a = acc_init();
+    const float slack = k > 0.0f ? kRefSlack / k : 0.0f;
+    for (int64_t c0 = sg.s0; c0 < sg.sf; c0 += kChunkVecs, ++g) {
+      const int n = static_cast<int>(sg.sf - c0 < kChunkVecs ? sg.sf - c0 : kChunkVecs);
+      const int st = g % kStages;
+      if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs)) {
+        sm.abort = 1;
+        atomicOr(ws.err, 1u);
+      } else if (k > 0.0f) {
+        fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), static_cast<int32_t>(c0), n, k, slack);
+      } else {
+        fold_stage<DT, false>(a, smem_addr(&sm.buf[st][0]), static_cast<int32_t>(c0), n, k, slack);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));
+    }
+    if (threadIdx.x == 0 && sg.s1 > nfull && nfull >= sg.s0) {  // the row's ragged tail vector
+      if (k > 0.0f) {
+        fold_tail<DT, true>(a, lg, row, nfull, k);
+      } else {
+        fold_tail<DT, false>(a, lg, row, nfull, k);
       }
     }
-    __syncthreads();
+    // hand the statistics to the finalizer and go on with the next row
+    const int slot = i & 1;
+    if (!mbar_wait_bounded(smem_addr(&sm.seg_empty[slot]), ((i >> 1) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
+      sm.abort = 1;
+      atomicOr(ws.err, 1u);
+    }
+    sm.seg[slot][threadIdx.x] = SegSlot{a.m, k > 0.0f ? acc_sum_at_max(a, k) : 0.0f, a.vidx, a.idx, a.flags};
+    mbar_arrive(smem_addr(&sm.seg_full[slot]));
   }
 }
 
@@ -286,7 +485,7 @@ __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float
   out_max[row] = st.M;
   out_argmax[row] = st.argmax;
   out_z[row] = st.Z;
-  if (row_flags) row_flags[row] = st.flags;
+  if (row_flags) row_flags[row] = st.flags | (__ldcg(ws.err) ? kStTimeout : 0u);
   if (out_p) {
     float p = 0.0f;
     if (probe && st.k > 0.0f && st.argmax >= 0) {
@@ -303,9 +502,19 @@ __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float
 }  // namespace
 
 cudaError_t stats_occupancy(int dtype, int* blocks_per_sm) {
-  if (dtype == SV_BF16)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_BF16>, kStatsThreads, 0);
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_F32>, kStatsThreads, 0);
+  cudaError_t e;
+  if (dtype == SV_BF16) {
+    e = cudaFuncSetAttribute(k_row_stats<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kStatsSmemBytes));
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_BF16>, kStatsThreads,
+                                                         kStatsSmemBytes);
+  }
+  e = cudaFuncSetAttribute(k_row_stats<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kStatsSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_F32>, kStatsThreads,
+                                                       kStatsSmemBytes);
 }
 
 int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
@@ -314,7 +523,7 @@ int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
   const int64_t NV = NVr * lg.rows;
   // One resident wave; at least ~2 vectors per thread per CTA; never more CTAs than vectors.
   int64_t g = static_cast<int64_t>(dev.sms) * dev.stats_blocks_per_sm[lg.dtype == SV_BF16 ? 1 : 0];
-  const int64_t by_work = (NV + 2 * kStatsThreads - 1) / (2 * kStatsThreads);
+  const int64_t by_work = (NV + 2 * kConsumers - 1) / (2 * kConsumers);
   if (g > by_work) g = by_work;
   if (g > kMaxStatsGrid) g = kMaxStatsGrid;
   if (g > NV) g = NV;
@@ -327,9 +536,9 @@ cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& 
   const int64_t NVr = (lg.vocab + E - 1) / E;
   const int64_t NV = NVr * lg.rows;
   if (lg.dtype == SV_BF16) {
-    k_row_stats<SV_BF16><<<grid, kStatsThreads, 0, stream>>>(lg, map, ws, NVr, NV);
+    k_row_stats<SV_BF16><<<grid, kStatsThreads, kStatsSmemBytes, stream>>>(lg, map, ws, NVr, NV);
   } else {
-    k_row_stats<SV_F32><<<grid, kStatsThreads, 0, stream>>>(lg, map, ws, NVr, NV);
+    k_row_stats<SV_F32><<<grid, kStatsThreads, kStatsSmemBytes, stream>>>(lg, map, ws, NVr, NV);
   }
   return cudaGetLastError();
 }

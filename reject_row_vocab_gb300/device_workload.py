@@ -17,6 +17,19 @@ _ARRAYS = ("cu_seqlens", "verify_ids", "q", "temperature", "u_accept", "u_final"
            "first_child", "next_sibling", "row_slots", "seq_lens")
 
 
+def padded_rows(t: torch.Tensor, device) -> torch.Tensor:
+    """A [rows, V] device view whose row stride is a multiple of 16 bytes (the library's layout rule)."""
+    rows, V = t.shape
+    per = 16 // t.element_size()
+    ld = (V + per - 1) // per * per
+    if ld == V:
+        return t.to(device)
+    buf = torch.zeros((rows, ld), dtype=t.dtype, device=device)
+    view = buf[:, :V]
+    view.copy_(t)
+    return view
+
+
 def _to_tensor(a: np.ndarray) -> torch.Tensor:
     if a.dtype == np.uint16:
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
@@ -39,7 +52,12 @@ class DeviceInputs:
             if v is not None:
                 d.t[k] = _to_tensor(v)
         for k, v in d.t.items():
-            d.t[k] = v.pin_memory() if pin else v.to(device)
+            if pin:
+                d.t[k] = v.pin_memory()
+            elif k in ("logits", "q"):
+                d.t[k] = padded_rows(v, device)
+            else:
+                d.t[k] = v.to(device)
         return d
 
     def __getitem__(self, k):

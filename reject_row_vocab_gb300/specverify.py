@@ -25,7 +25,8 @@ DEV_TOKEN_RANGE, DEV_NONFINITE, DEV_BAD_TREE, DEV_BAD_LAYOUT, DEV_RESIDUAL_EMPTY
 
 ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spec_verify_greedy_chain",
                 "spec_verify_greedy_tree", "spec_verify_rejection_chain", "spec_verify_rejection_ragged",
-                "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events")
+                "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events",
+                "spec_verify_last_cuda_error")
 
 
 class SpecVerifyError(RuntimeError):
@@ -56,6 +57,7 @@ def load_library():
     sig = {
         "spec_verify_workspace_bytes": ([I64, I32, I32, I32], SZ),
         "spec_verify_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "spec_verify_last_cuda_error": ([], ctypes.c_char_p),
         "spec_verify_greedy_chain": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, OUT, P, SZ, P], ctypes.c_int),
         "spec_verify_greedy_tree": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, P, P, P, OUT, P, SZ, P],
                                     ctypes.c_int),
@@ -95,7 +97,11 @@ def _dtype(logits: torch.Tensor) -> int:
 
 def _check(fn: str, code: int):
     if code != 0:
-        raise SpecVerifyError(fn, code, load_library().spec_verify_status_string(code).decode())
+        lib = load_library()
+        msg = lib.spec_verify_status_string(code).decode()
+        if code == 7:
+            msg += " (%s)" % lib.spec_verify_last_cuda_error().decode()
+        raise SpecVerifyError(fn, code, msg)
 
 
 def set_stats_events(start=None, stop=None):
