@@ -196,6 +196,33 @@ sv_status_t spec_verify_target_only_tree(const void* logits, sv_dtype_t dtype, i
                                          const sv_out_t* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * p/q rejection chain without a caller workspace.  (The pages have no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * For callers that cannot provide device scratch memory — for example a plugin
+ * that its host framework hands only input and output buffers, code that runs
+ * after a serving engine has reserved all device memory for itself, or an
+ * embedding that must not allocate at call time.  Same arguments and results as
+ * spec_verify_rejection_chain, minus ws / ws_bytes: the library uses one fixed
+ * scratch area of SV_NOALLOC_SCRATCH_BYTES bytes in its own device image (every
+ * GPU that uses the library keeps it until the process exits) and allocates
+ * nothing.  Problems whose workspace would exceed that size
+ * (spec_verify_workspace_bytes(batch*(m+1), batch, vocab, m+1) >
+ * SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE_TOO_SMALL before anything is
+ * enqueued.  The first call on each device looks up the area's device address;
+ * make it before any stream capture starts.  Every call clears the area's
+ * counters on `stream` before launching; all calls share the area, so calls
+ * that overlap on the GPU (other streams or host threads) race — serialise them.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+sv_status_t spec_verify_rejection_chain_noalloc(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                                int32_t m, int32_t vocab, const int32_t* verify_ids, const float* q,
+                                                int64_t ldq, const float* temperature, const float* u_accept,
+                                                const float* u_final, const int64_t* row_slots,
+                                                const int64_t* seq_lens, const sv_out_t* out, cudaStream_t stream);
+
+/*
  * Row statistics on their own (the single pass every entry point starts
  * with): for each of `rows` rows, the maximum M (float), the lowest argmax
  * (-1 for an all -inf row), Z = sum_v exp((l_v - M)/T) with T = row_temp[row]
