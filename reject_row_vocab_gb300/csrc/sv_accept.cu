@@ -29,10 +29,9 @@ constexpr int kChainWarps = 4;
 __device__ __forceinline__ uint32_t warp_or(uint32_t v) { return __reduce_or_sync(kFull, v); }
 
 // p_row(token) from the row statistics; 0 for an excluded (NaN / +inf) entry.
-__device__ __forceinline__ double target_prob(const LogitsView& lg, int64_t row, int32_t tok, const RowStat& rs) {
-  const float l = load_logit(lg, row, tok);
-  if (!usable_logit(l)) return 0.0;
-  return static_cast<double>(exp2f((l - rs.M) * rs.k)) / rs.Z;
+__device__ __forceinline__ float target_prob(float l, const RowStat& rs) {
+  if (!usable_logit(l)) return 0.0f;
+  return __fdiv_rn(exp2f((l - rs.M) * rs.k), rs.Z);
 }
 
 __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
@@ -97,10 +96,9 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
         stop = (rs.argmax != d) ? 1 : 0;
       } else {
         const float l = load_logit(p.lg, row, d);
-        const double qd = static_cast<double>(p.q[row * p.ldq + d]);
-        const double pd = usable_logit(l) ? static_cast<double>(exp2f((l - rs.M) * rs.k)) / rs.Z : 0.0;
-        const double u = static_cast<double>(p.u_accept[row]);
-        stop = (u * qd < pd) ? 0 : 1;
+        const float qd = p.q[row * p.ldq + d];
+        const float u = p.u_accept[row];
+        stop = (__fmul_rn(u, qd) < target_prob(l, rs)) ? 0 : 1;
       }
     }
     const unsigned bal = __ballot_sync(kFull, tested && stop != 0);
@@ -161,7 +159,7 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
   __shared__ int32_t s_tok[kMaxNodes];
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ int32_t s_kid[kMaxNodes];
-  __shared__ double s_pk[kMaxNodes];
+  __shared__ float s_pk[kMaxNodes];
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
   const int N = p.nodes;
@@ -261,13 +259,12 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
     } else {
       for (int kk = lane; kk < nk; kk += 32) {
         const int32_t t = s_tok[s_kid[kk]];
-        s_pk[kk] = (t >= 0 && t < V) ? target_prob(p.lg, row, t, rs) : 0.0;
+        s_pk[kk] = (t >= 0 && t < V) ? target_prob(load_logit(p.lg, row, t), rs) : 0.0f;
       }
       __syncwarp();
       if (lane == 0) {
-        const double u = static_cast<double>(p.u_accept[row]);
-        const double th_acc = static_cast<double>(p.th_acc), th_single = static_cast<double>(p.th_single);
-        double c = 0.0;
+        const float u = p.u_accept[row];
+        float c = 0.0f;
         int32_t* excl = ws.excl + static_cast<int64_t>(b) * N;
         for (int kk = 0; kk < nk; ++kk) {
           const int32_t t = s_tok[s_kid[kk]];
@@ -282,9 +279,9 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
             continue;
           }
           excl[n_excl++] = t;
-          const double pk = s_pk[kk];
-          c += pk;
-          if (u < c / th_acc || pk >= th_single) {
+          const float pk = s_pk[kk];
+          c = __fadd_rn(c, pk);
+          if (u < __fdiv_rn(c, p.th_acc) || pk >= p.th_single) {
             next = s_kid[kk];
             break;
           }

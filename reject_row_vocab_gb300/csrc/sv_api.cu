@@ -85,7 +85,7 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   w->partial = reinterpret_cast<RowPartial*>(base + L.partial);
   w->state = reinterpret_cast<ReqState*>(base + L.state);
   w->excl = reinterpret_cast<int32_t*>(base + L.excl);
-  w->tsum = reinterpret_cast<double*>(base + L.tsum);
+  w->tsum = reinterpret_cast<uint64_t*>(base + L.tsum);
   w->ntiles = L.ntiles;
   return SV_OK;
 }

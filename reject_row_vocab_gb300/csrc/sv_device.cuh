@@ -108,6 +108,16 @@ __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   return r;
 }
 
+// Ticket on a counter at GPU scope with release and acquire semantics: the
+// caller's earlier writes (and, through a preceding barrier, its block's) are
+// visible before the increment, and reads after it see the writes other
+// arrivals made before theirs.
+__device__ __forceinline__ unsigned ticket_add(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Barrier among the first `threads` threads of the block (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int threads) { asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory"); }
 
@@ -236,66 +246,56 @@ __device__ __forceinline__ Part part_reduce_named(Part p, float k, Part* smem /*
   return p;
 }
 
-// Cross-CTA partial in double: (m, s, idx, flags).
-struct PartD {
-  float m;
-  double s;
-  int32_t idx;
-  uint32_t flags;
-};
-
-__device__ __forceinline__ PartD partd_identity() { return PartD{-kInfF, 0.0, -1, 0u}; }
-
-__device__ __forceinline__ void partd_merge(PartD& a, const PartD& b, float k) {
-  const float M = fmaxf(a.m, b.m);
-  int32_t idx;
-  if (a.m > b.m) {
-    idx = a.idx;
-  } else if (b.m > a.m) {
-    idx = b.idx;
-  } else {
-    idx = min(a.idx, b.idx);
-  }
-  double s = 0.0;
-  if (k > 0.0f && M > -kInfF) {
-    if (a.m == M) {
-      s += a.s;
-    } else if (a.s != 0.0) {
-      s += a.s * static_cast<double>(exp2f((a.m - M) * k));
-    }
-    if (b.m == M) {
-      s += b.s;
-    } else if (b.s != 0.0) {
-      s += b.s * static_cast<double>(exp2f((b.m - M) * k));
-    }
-  }
-  a.m = M;
-  a.s = s;
-  a.idx = idx;
-  a.flags |= b.flags;
-}
-
-__device__ __forceinline__ PartD partd_warp_reduce(PartD p, float k) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    PartD o;
-    o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
-    o.s = __shfl_xor_sync(0xffffffffu, p.s, off);
-    o.idx = __shfl_xor_sync(0xffffffffu, p.idx, off);
-    o.flags = __shfl_xor_sync(0xffffffffu, p.flags, off);
-    partd_merge(p, o, k);
-  }
-  return p;
-}
-
 // Coherent (L2) loads of a partial written by another CTA.
-__device__ __forceinline__ PartD load_partial_cg(const RowPartial* rp) {
-  PartD p;
+__device__ __forceinline__ Part load_partial_cg(const RowPartial* rp) {
+  Part p;
   p.s = __ldcg(&rp->s);
   p.m = __ldcg(&rp->m);
   p.idx = __ldcg(&rp->idx);
   p.flags = __ldcg(&rp->flags);
   return p;
+}
+
+// x >= 0 (a sum of sampling weights, below 2^18) as fixed point with
+// kFixedBits fractional bits, rounded to nearest; monotone in x.
+__device__ __forceinline__ uint64_t to_fixed(float x) {
+  const uint32_t bits = __float_as_uint(x);
+  const int e = static_cast<int>((bits >> 23) & 0xffu);
+  if (e == 0) return 0ull;  // zero (and sub-normals, far below one unit)
+  const uint64_t mant = static_cast<uint64_t>((bits & 0x7fffffu) | 0x800000u);
+  const int sh = e - 127 - 23 + kFixedBits;  // value = mant * 2^sh
+  if (sh >= 0) return mant << sh;
+  if (sh <= -25) return 0ull;
+  return (mant + (1ull << (-sh - 1))) >> (-sh);
+}
+
+// floor(u * S) for u in [0, 1) (any fp32) and a fixed-point total S < 2^62.
+__device__ __forceinline__ uint64_t scale_fixed(float u, uint64_t S) {
+  const uint32_t bits = __float_as_uint(u);
+  const int e = static_cast<int>((bits >> 23) & 0xffu);
+  if (e == 0 || (bits >> 31)) return 0ull;  // zero, sub-normal or negative
+  const uint64_t mant = static_cast<uint64_t>((bits & 0x7fffffu) | 0x800000u);
+  const int sh = 127 + 23 - e;  // u = mant * 2^-sh, sh >= 24 for u < 1
+  const uint64_t lo = mant * S, hi = __umul64hi(mant, S);
+  if (sh >= 128) return 0ull;
+  if (sh >= 64) return hi >> (sh - 64);
+  return (hi << (64 - sh)) | (lo >> sh);
+}
+
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+__device__ __forceinline__ uint64_t warp_inclusive_scan_u64(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint64_t t = __shfl_up_sync(0xffffffffu, v, off);
+    if (lane >= off) v += t;
+  }
+  return v;
 }
 
 // Warp-wide inclusive scan of doubles in lane order.

@@ -24,26 +24,31 @@ constexpr uint32_t kStTimeout = SV_DEV_TIMEOUT;
 
 // Final statistics of one logits row, written by the row-statistics kernel.
 // M is the row maximum over usable entries (finite or -inf), argmax its lowest
-// index (-1 for an all -inf row), k = log2(e)/T (0 for a greedy row) and
-// Z = sum_v 2^((l_v - M) * k) (0 for a greedy row).
+// index (-1 for an all -inf row), k = log2(e)/T (0 for a greedy row),
+// Z = sum_v 2^((l_v - M) * k) and inv_z = 1/Z (both 0 for a greedy row).
 struct RowStat {
-  double Z;
+  float Z;
   float M;
   int32_t argmax;
   uint32_t flags;
   float k;
+  float inv_z;
 };
 static_assert(sizeof(RowStat) == 24, "RowStat layout");
 
 // A CTA's partial statistics for the part of one row it scanned.
 struct RowPartial {
-  double s;  // sum of 2^((l - m) * k) over the part
+  float s;  // sum of 2^((l - m) * k) over the part
   float m;
   int32_t idx;
   uint32_t flags;
-  uint32_t pad;
 };
-static_assert(sizeof(RowPartial) == 24, "RowPartial layout");
+static_assert(sizeof(RowPartial) == 16, "RowPartial layout");
+
+// Sampling weights are summed as exact 64-bit fixed-point integers with 44
+// fractional bits (a lane's sum of eight weights is below 2^4, a row's total
+// below 2^62), so prefix sums do not depend on the order of the additions.
+constexpr int kFixedBits = 44;
 
 // What the final-token step has to do for a request.
 enum SampleMode : int32_t {
@@ -102,7 +107,7 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
                            static_cast<size_t>(max_len > 0 ? max_len : 1), 256);
   L.ntiles = (vocab + kTile - 1) / kTile;
   L.tsum = off;
-  off = align_up(off + sizeof(double) * static_cast<size_t>(batch > 0 ? batch : 1) *
+  off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
                            static_cast<size_t>(L.ntiles > 0 ? L.ntiles : 1), 256);
   L.total = off;
   return L;
@@ -118,7 +123,7 @@ struct Ws {
   RowPartial* partial;
   ReqState* state;
   int32_t* excl;
-  double* tsum;
+  uint64_t* tsum;  // fixed-point tile sums of the sampled rows
   int32_t ntiles;
 };
 

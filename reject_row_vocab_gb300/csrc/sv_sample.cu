@@ -140,7 +140,7 @@ __device__ __forceinline__ float lane_sum(const float (&w)[8]) {
   return s;
 }
 
-__device__ __forceinline__ float inverse_z(const RowStat& rs) { return static_cast<float>(1.0 / rs.Z); }
+__device__ __forceinline__ float inverse_z(const RowStat& rs) { return rs.inv_z; }
 
 // Barrier over the first BS threads: the named barrier when a producer warp
 // beyond them must not take part, else the whole block.
@@ -231,7 +231,7 @@ __device__ __forceinline__ void commit_block_named(const OutView& out, const Com
 template <int DT, bool RESID>
 __device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
                                                  const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
-                                                 int32_t n_excl, int ta, int tb, double* ts) {
+                                                 int32_t n_excl, int ta, int tb, uint64_t* ts) {
   constexpr int U = 4;
   const int lane = threadIdx.x & 31;
   const int full_tiles = lg.vocab / kTile;
@@ -283,22 +283,25 @@ __device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const flo
         }
       }
     }
+    uint64_t fx[U];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {  // U butterflies, interleaved
+    for (int u = 0; u < U; ++u) fx[u] = to_fixed(ls[u]);
 #pragma unroll
-      for (int u = 0; u < U; ++u) ls[u] += __shfl_xor_sync(0xffffffffu, ls[u], off);
+    for (int off = 16; off > 0; off >>= 1) {  // U exact butterflies, interleaved
+#pragma unroll
+      for (int u = 0; u < U; ++u) fx[u] += __shfl_xor_sync(0xffffffffu, fx[u], off);
     }
     if (lane == 0) {
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (t0 + u < tb) ts[t0 + u] = static_cast<double>(ls[u]);
+        if (t0 + u < tb) ts[t0 + u] = fx[u];
     }
   }
 }
 
 __device__ __forceinline__ void warp_tile_sums(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
                                                const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
-                                               int32_t n_excl, int ta, int tb, double* ts) {
+                                               int32_t n_excl, int ta, int tb, uint64_t* ts) {
   const bool resid = mode == kModeResidual;
   if (lg.dtype == SV_BF16) {
     if (resid) {
@@ -316,54 +319,54 @@ __device__ __forceinline__ void warp_tile_sums(const LogitsView& lg, const float
 }
 
 // The draw of one request by one CTA, once all its tile sums exist: scan the
-// tile sums, pick the tile holding t = u_final * S, then one warp re-forms
-// that tile's weights (same arithmetic as the sums) and walks to the entry.
+// (exact, fixed-point) tile sums, pick the tile holding T = floor(u_final * S),
+// then one warp re-forms that tile's weights (same arithmetic as the sums) and
+// walks to the entry.  rs is the sampled row's statistics, u its uniform.
 template <bool NAMED>
-__device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
+__device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q, int64_t ldq, float u,
                                            const OutView& out, const CommitParams& cp, const Ws& ws,
-                                           int32_t excl_stride, int b, const ReqState& rq) {
-  __shared__ double s_scan[kSampleWarps + 1];
+                                           int32_t excl_stride, int b, const ReqState& rq, const RowStat& rs) {
+  __shared__ uint64_t s_scan[kSampleWarps + 1];
   __shared__ int s_tile;
   __shared__ int s_last_nz;
-  __shared__ double s_pre;
+  __shared__ uint64_t s_pre;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = ws.ntiles;
   const int64_t row = rq.sample_row;
-  const RowStat rs = ws.rowstat[row];
   const float inv_z = inverse_z(rs);
   const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
-  double* ts = ws.tsum + static_cast<int64_t>(b) * T;
+  uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
   int32_t mode = rq.mode;
   uint32_t st_add = 0u;
   const int per = (T + kSampleThreads - 1) / kSampleThreads;
   const int ta = min(T, tid * per), tb = min(T, ta + per);
 
-  double loc = 0.0;
-  for (int j = ta; j < tb; ++j) loc += __ldcg(ts + j);
-  double total;
-  double pre = block_exclusive_scan<double, kSampleThreads, NAMED>(loc, s_scan, &total);
-  if (!(total > 0.0)) {  // residual (or what is left of p) is empty: draw from p instead
+  uint64_t loc = 0;
+  for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+  uint64_t total;
+  uint64_t pre = block_exclusive_scan<uint64_t, kSampleThreads, NAMED>(loc, s_scan, &total);
+  if (total == 0) {  // residual (or what is left of p) is empty: draw from p instead
     mode = kModeP;
     st_add = kStResidualEmpty;
     warp_tile_sums(lg, q, ldq, row, rs, inv_z, mode, excl, 0, warp * ((T + kSampleWarps - 1) / kSampleWarps),
                    min(T, (warp + 1) * ((T + kSampleWarps - 1) / kSampleWarps)), ts);
     __threadfence_block();
     group_sync<kSampleThreads, NAMED>();
-    loc = 0.0;
-    for (int j = ta; j < tb; ++j) loc += __ldcg(ts + j);
-    pre = block_exclusive_scan<double, kSampleThreads, NAMED>(loc, s_scan, &total);
+    loc = 0;
+    for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    pre = block_exclusive_scan<uint64_t, kSampleThreads, NAMED>(loc, s_scan, &total);
   }
-  const double t = static_cast<double>(u_final[b]) * total;
+  const uint64_t t = scale_fixed(u, total);
   if (tid == 0) {
     s_tile = INT_MAX;
     s_last_nz = -1;
   }
   group_sync<kSampleThreads, NAMED>();
   int my_tile = INT_MAX, my_nz = -1;
-  double my_pre = 0.0, run = pre;
+  uint64_t my_pre = 0, run = pre;
   for (int j = ta; j < tb; ++j) {
-    const double wj = __ldcg(ts + j);
-    if (wj > 0.0) {
+    const uint64_t wj = __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    if (wj > 0) {
       my_nz = j;
       if (my_tile == INT_MAX && run <= t && t < run + wj) {
         my_tile = j;
@@ -383,22 +386,22 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   int v = -1;
   if (located || s_last_nz >= 0) {
     const int tile = located ? s_tile : s_last_nz;
-    const double tpre = located ? s_pre : 0.0;
+    const uint64_t tpre = located ? s_pre : 0;
     const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
     float w[8];
     lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, mode == kModePExcl ? rq.n_excl : 0, col0, w);
-    const double ls = static_cast<double>(lane_sum(w));
-    const double li = warp_inclusive_scan(ls);
-    const double lo = tpre + (li - ls), hi = tpre + li;
-    const unsigned hit = __ballot_sync(0xffffffffu, located && ls > 0.0 && lo <= t && t < hi);
+    const uint64_t W = to_fixed(lane_sum(w));
+    const uint64_t li = warp_inclusive_scan_u64(W);
+    const uint64_t lo = tpre + (li - W), hi = tpre + li;
+    const unsigned hit = __ballot_sync(0xffffffffu, located && W > 0 && lo <= t && t < hi);
     if (hit) {
       const int f = __ffs(hit) - 1;
       int cand = -1;
       if (lane == f) {
-        float cum = 0.0f;  // the same fp32 additions as lane_sum
+        float cum = 0.0f;  // the same fp32 additions as lane_sum, so the last step reaches W
         for (int i = 0; i < 8; ++i) {
           cum = __fadd_rn(cum, w[i]);
-          if (cand < 0 && lo + static_cast<double>(cum) > t) cand = i;
+          if (cand < 0 && lo + to_fixed(cum) > t) cand = i;
         }
         if (cand < 0)
           for (int i = 7; i >= 0; --i)
@@ -406,8 +409,8 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
       }
       cand = __shfl_sync(0xffffffffu, cand, f);
       v = static_cast<int>(static_cast<int64_t>(tile) * kTile + f * 8 + cand);
-    } else {  // rounding left t outside every lane: last positive entry of the tile
-      const unsigned nz = __ballot_sync(0xffffffffu, ls > 0.0);
+    } else {  // not reachable with exact sums; kept as a defined outcome: last positive entry of the tile
+      const unsigned nz = __ballot_sync(0xffffffffu, W > 0);
       const int f = nz ? 31 - __clz(nz) : 0;
       int cand = -1;
       if (lane == f)
@@ -540,8 +543,9 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     const int64_t row = rq.sample_row;
     const RowStat rs = ws.rowstat[row];
     const float inv_z = inverse_z(rs);
+    const float u = u_final[b];
     const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
-    double* ts = ws.tsum + static_cast<int64_t>(b) * T;
+    uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
     for (int c0 = ta; c0 < tc; c0 += per, ++g) {
       const int n = min(per, tc - c0);
       const int st = g % kSampleStages;
@@ -564,10 +568,8 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
           lane_unpack(r, lg.dtype, resid, x, qv);
           weights_from_values(x, qv, rs, inv_z, rq.mode, excl, rq.n_excl,
                               static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
-          float ls = lane_sum(w);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-          if (lane == 0) ts[c0 + i] = static_cast<double>(ls);
+          const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
+          if (lane == 0) ts[c0 + i] = fx;
         }
       }
       __syncwarp();
@@ -577,21 +579,17 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
       float w[8];
       lane_weights(lg, q, ldq, row, rs, inv_z, rq.mode, excl, rq.n_excl, static_cast<int64_t>(tile) * kTile + lane * 8,
                    w);
-      float ls = lane_sum(w);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-      if (lane == 0) ts[tile] = static_cast<double>(ls);
+      const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
+      if (lane == 0) ts[tile] = fx;
     }
     named_sync(kSampleThreads);
     if (threadIdx.x == 0) {
-      __threadfence();
       const unsigned add = static_cast<unsigned>(tb - ta);
-      ring.last = (atomicAdd(&ws.chunk_cnt[b], add) + add == static_cast<unsigned>(T));
+      ring.last = (ticket_add(&ws.chunk_cnt[b], add) + add == static_cast<unsigned>(T));
     }
     named_sync(kSampleThreads);
     if (ring.last) {
-      __threadfence();
-      block_draw<true>(lg, q, ldq, u_final, out, cp, ws, excl_stride, static_cast<int>(b), rq);
+      block_draw<true>(lg, q, ldq, u, out, cp, ws, excl_stride, static_cast<int>(b), rq, rs);
       if (threadIdx.x == 0) ws.chunk_cnt[b] = 0u;  // leave the counter clean for the next call
       named_sync(kSampleThreads);
     }

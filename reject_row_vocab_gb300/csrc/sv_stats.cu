@@ -281,6 +281,19 @@ __device__ __forceinline__ int64_t cta_of_vector(int64_t v, int64_t G, int64_t N
   return ((v + 1) * G - 1) / NV;
 }
 
+// The row's final statistics from its merged partial.
+__device__ __forceinline__ RowStat finish_row(const Part& p, float k) {
+  RowStat st;
+  const bool samp = k > 0.0f && p.m > -kInfF;
+  st.Z = samp ? p.s : 0.0f;
+  st.inv_z = samp ? __fdiv_rn(1.0f, p.s) : 0.0f;
+  st.M = p.m;
+  st.argmax = p.idx;
+  st.flags = p.flags;
+  st.k = k;
+  return st;
+}
+
 // Segment geometry of one row within a CTA's range.
 struct Seg {
   int64_t s0, s1, sf;  // vectors [s0, s1) of the row are ours; [s0, sf) are full vectors
@@ -388,47 +401,30 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       const int64_t c_lo = cta_of_vector(row * NVr, G, NV);
       const int64_t c_hi = cta_of_vector(row * NVr + NVr - 1, G, NV);
       if (c_lo == c_hi) {  // the whole row is ours
-        if (lane == 0) {
-          RowStat st;
-          st.Z = (k > 0.0f && p.m > -kInfF) ? static_cast<double>(p.s) : 0.0;
-          st.M = p.m;
-          st.argmax = p.idx;
-          st.flags = p.flags;
-          st.k = k;
-          ws.rowstat[row] = st;
-        }
+        if (lane == 0) ws.rowstat[row] = finish_row(p, k);
         continue;
       }
       int last = 0;
       if (lane == 0) {
         RowPartial rp;
-        rp.s = static_cast<double>(p.s);
+        rp.s = p.s;
         rp.m = p.m;
         rp.idx = p.idx;
         rp.flags = p.flags;
-        rp.pad = 0u;
         ws.partial[2 * c + (row == r_first ? 0 : 1)] = rp;
-        __threadfence();
-        const unsigned ticket = atomicAdd(&ws.row_cnt[row], 1u);
+        const unsigned ticket = ticket_add(&ws.row_cnt[row], 1u);
         last = (ticket == static_cast<unsigned>(c_hi - c_lo));
       }
       if (__shfl_sync(0xffffffffu, last, 0)) {  // last arriver: merge the row's partials in CTA order
-        __threadfence();
-        PartD acc = partd_identity();
+        __syncwarp();
+        Part acc = part_identity();
         for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32) {
           const int64_t first_row_cc = (cc * NV / G) / NVr;
-          const PartD q = load_partial_cg(&ws.partial[2 * cc + (row == first_row_cc ? 0 : 1)]);
-          partd_merge(acc, q, k);
+          part_merge(acc, load_partial_cg(&ws.partial[2 * cc + (row == first_row_cc ? 0 : 1)]), k);
         }
-        acc = partd_warp_reduce(acc, k);
+        acc = part_warp_reduce(acc, k);
         if (lane == 0) {
-          RowStat st;
-          st.Z = (k > 0.0f && acc.m > -kInfF) ? acc.s : 0.0;
-          st.M = acc.m;
-          st.argmax = acc.idx;
-          st.flags = acc.flags;
-          st.k = k;
-          ws.rowstat[row] = st;
+          ws.rowstat[row] = finish_row(acc, k);
           ws.row_cnt[row] = 0u;  // leave the counter clean for the next call
         }
       }
@@ -492,7 +488,7 @@ __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float
       const int32_t t = probe[row];
       if (t >= 0 && t < lg.vocab) {
         const float l = load_logit(lg, row, t);
-        if (usable_logit(l)) p = static_cast<float>(static_cast<double>(exp2f((l - st.M) * st.k)) / st.Z);
+        if (usable_logit(l)) p = __fdiv_rn(exp2f((l - st.M) * st.k), st.Z);
       }
     }
     out_p[row] = p;
