@@ -35,6 +35,8 @@ __device__ __forceinline__ float target_prob(float l, const RowStat& rs) {
 }
 
 __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
+  grid_dependency_wait();  // row statistics from the previous kernel
+  allow_dependents();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * kChainWarps + (threadIdx.x >> 5);
   if (b >= p.batch) return;
@@ -160,6 +162,8 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ int32_t s_kid[kMaxNodes];
   __shared__ float s_pk[kMaxNodes];
+  grid_dependency_wait();  // row statistics from the previous kernel
+  allow_dependents();
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
   const int N = p.nodes;
@@ -322,13 +326,11 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
 
 cudaError_t launch_accept_chain(const ChainParams& p, const OutView& out, const Ws& ws, cudaStream_t stream) {
   const int blocks = (p.batch + kChainWarps - 1) / kChainWarps;
-  k_accept_chain<<<blocks, 32 * kChainWarps, 0, stream>>>(p, out, ws);
-  return cudaGetLastError();
+  return launch_pdl(k_accept_chain, dim3(blocks), dim3(32 * kChainWarps), 0, stream, p, out, ws);
 }
 
 cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws& ws, cudaStream_t stream) {
-  k_accept_tree<<<p.batch, 32, 0, stream>>>(p, out, ws);
-  return cudaGetLastError();
+  return launch_pdl(k_accept_tree, dim3(p.batch), dim3(32), 0, stream, p, out, ws);
 }
 
 }  // namespace sv

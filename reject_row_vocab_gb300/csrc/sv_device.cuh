@@ -12,7 +12,6 @@
 namespace sv {
 
 constexpr float kInfF = __builtin_huge_valf();
-constexpr double kLog2eD = 1.4426950408889634074;
 
 // ---------------------------------------------------------------------------
 // Loads
@@ -62,6 +61,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Announce `bytes` of incoming bulk-copy data without arriving (the arrival
+// comes later, once the stage's description is written).
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -80,18 +85,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for the phase of `bar` with the given parity, for at most `limit_ns`;
-// gives up early once *abort is set.  Returns false if it gave up.
+// Wait for the phase of `bar` with the given parity, for at most about
+// `limit_ns`; gives up early once *abort is set.  Returns false if it gave up.
+// Between polls the warp sleeps about `sleep_ns` (0: poll back to back):
+// warps that poll without pause take issue slots from the warps doing work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t limit_ns) {
+                                                  uint64_t limit_ns, uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t spin = 1;; ++spin) {
+  for (;;) {
+    if (sleep_ns) __nanosleep(sleep_ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 63u) == 0u) {
-      if (*abort) return false;
-      if (global_ns() - t0 > limit_ns) return false;
-    }
+    if (*abort) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -102,11 +108,22 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
+// Start pulling `bytes` (a multiple of 16, 16-byte aligned) into L2 without waiting.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   uint4 r;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
   return r;
 }
+
+// Programmatic dependent launch: wait until the kernels this one depends on
+// (earlier work on the stream) have completed and their writes are visible;
+// and let the next kernel on the stream begin launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Ticket on a counter at GPU scope with release and acquire semantics: the
 // caller's earlier writes (and, through a preceding barrier, its block's) are
@@ -147,10 +164,18 @@ __device__ __forceinline__ float ex2_fast(float x) {
 
 __device__ __forceinline__ bool usable_logit(float x) { return !(x != x) && x != kInfF; }
 
-// log2(e)/T rounded once to fp32, or 0 for a greedy temperature.
+// log2(e)/T in fp32, or 0 for a greedy temperature.  log2(e) is split into
+// a head and a tail float; the head's quotient is corrected with its exact
+// remainder (one fused multiply-add), which brings the result within an ulp
+// of the exact quotient without fp64 (whose dependent latency is long here).
 __device__ __forceinline__ float temperature_k(float T) {
   const bool sampling = (T >= 1e-30f) && (T < kInfF);
-  return sampling ? static_cast<float>(kLog2eD / static_cast<double>(T)) : 0.0f;
+  if (!sampling) return 0.0f;
+  constexpr float kHi = 1.44269502162933349609375f;  // fp32 nearest to log2(e)
+  constexpr float kLo = 1.925963033500011e-08f;      // log2(e) - kHi
+  const float q = __fdiv_rn(kHi, T);
+  const float r = fmaf(-q, T, kHi) + kLo;  // remainder of the head (exact) plus the tail
+  return fmaf(r, __frcp_rn(T), q);
 }
 
 __device__ __forceinline__ bool sampling_temperature(float T) { return (T >= 1e-30f) && (T < kInfF); }

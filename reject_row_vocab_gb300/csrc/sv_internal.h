@@ -73,13 +73,11 @@ static_assert(sizeof(ReqState) == 32, "ReqState layout");
 
 // Elements per sampling tile (one warp, eight elements per lane).
 constexpr int kTile = 256;
-// Upper bound on the row-statistics grid (partial slots are sized for it).
-constexpr int kMaxStatsGrid = 4096;
 // Upper bound on tree nodes per request.
 constexpr int kMaxNodes = 1024;
 
 struct WsLayout {
-  size_t row_cnt, chunk_cnt, done_cnt, counters_end;
+  size_t chunk_cnt, done_cnt, counters_end;
   size_t rowstat, partial, state, excl, tsum, total;
   int32_t ntiles;
 };
@@ -89,8 +87,6 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len) {
   WsLayout L{};
   size_t off = 0;
-  L.row_cnt = off;
-  off += sizeof(uint32_t) * static_cast<size_t>(rows > 0 ? rows : 1);
   L.chunk_cnt = off;
   off += sizeof(uint32_t) * static_cast<size_t>(batch > 0 ? batch : 1);
   L.done_cnt = off;
@@ -98,8 +94,13 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
   L.counters_end = off = align_up(off, 256);
   L.rowstat = off;
   off = align_up(off + sizeof(RowStat) * static_cast<size_t>(rows > 0 ? rows : 1), 256);
-  L.partial = off;
-  off = align_up(off + sizeof(RowPartial) * 2 * kMaxStatsGrid, 256);
+  L.partial = off;  // one partial per chunk of a row (1024-vector chunks of fp32 rows bound every case)
+  {
+    const int64_t nfull = (vocab > 0 ? vocab : 1) / 4;
+    int64_t cpr = (nfull + 1023) / 1024;
+    if (cpr < 1) cpr = 1;
+    off = align_up(off + sizeof(RowPartial) * static_cast<size_t>(rows > 0 ? rows : 1) * static_cast<size_t>(cpr), 256);
+  }
   L.state = off;
   off = align_up(off + sizeof(ReqState) * static_cast<size_t>(batch > 0 ? batch : 1), 256);
   L.excl = off;
@@ -115,7 +116,6 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
 
 // Workspace pointers carved from the caller's buffer.
 struct Ws {
-  uint32_t* row_cnt;
   uint32_t* chunk_cnt;
   uint32_t* done_cnt;
   uint32_t* err;  // sticky error word: a bounded wait gave up (reported as SV_DEV_TIMEOUT)
@@ -199,6 +199,25 @@ struct CommitParams {
   const int64_t* seq_lens;
   uint32_t* err;  // workspace error word, cleared once the call's statuses carry it
 };
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous work on the stream drains, and waits for it (griddepcontrol)
+// before touching any memory that work produces.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Device properties cached per device.
 struct DeviceInfo {

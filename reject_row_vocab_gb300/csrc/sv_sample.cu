@@ -464,17 +464,20 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
                                                                    int32_t nblocks) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ SampleRing ring;
-  if (static_cast<int>(blockIdx.x) == nblocks) {  // the commit block
+  grid_dependency_wait();  // acceptance results from the previous kernel
+  allow_dependents();
+  if (blockIdx.x == 0) {  // the commit block (first, so it runs in the first wave)
     if (threadIdx.x < kCommitThreads) commit_block_named(out, cp);
     return;
   }
+  const int64_t blk = blockIdx.x - 1;
   unsigned char* stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                            ~uintptr_t(127));
   const int T = ws.ntiles;
   const int full_tiles = lg.vocab / kTile;
   const int es = lg.dtype == SV_BF16 ? 2 : 4;
   const int64_t total = static_cast<int64_t>(cp.batch) * T;
-  const int64_t t_begin = blockIdx.x * total / nblocks, t_end = (blockIdx.x + 1) * total / nblocks;
+  const int64_t t_begin = blk * total / nblocks, t_end = (blk + 1) * total / nblocks;
   if (t_begin >= t_end) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -596,7 +599,11 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
   }
 }
 
-__global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitParams cp) { commit_block(out, cp); }
+__global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitParams cp) {
+  grid_dependency_wait();  // acceptance results from the previous kernel
+  allow_dependents();
+  commit_block(out, cp);
+}
 
 }  // namespace
 
@@ -608,19 +615,18 @@ cudaError_t sample_smem_setup() {
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
                                      const DeviceInfo& dev, cudaStream_t stream) {
-  // one resident wave (two blocks per SM), at least ~16 tiles per block
+  // one resident wave (two blocks per SM, one slot for the commit block), at least ~16 tiles per block
   const int64_t tiles = static_cast<int64_t>(cp.batch) * ws.ntiles;
-  int64_t nblocks = static_cast<int64_t>(dev.sms) * 2;
+  int64_t nblocks = static_cast<int64_t>(dev.sms) * 2 - 1;
   if (nblocks > (tiles + 15) / 16) nblocks = (tiles + 15) / 16;
   if (nblocks < 1) nblocks = 1;
-  k_sample<<<static_cast<unsigned>(nblocks + 1), kSampleBlockThreads, kSampleSmemBytes, stream>>>(
-      lg, q, ldq, u_final, out, cp, ws, cp.max_len, static_cast<int32_t>(nblocks));
-  return cudaGetLastError();
+  return launch_pdl(k_sample, dim3(static_cast<unsigned>(nblocks + 1)), dim3(kSampleBlockThreads), kSampleSmemBytes,
+                    stream, lg, q, ldq, u_final, out, cp, ws, static_cast<int32_t>(cp.max_len),
+                    static_cast<int32_t>(nblocks));
 }
 
 cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream) {
-  k_commit<<<1, kCommitThreads, 0, stream>>>(out, cp);
-  return cudaGetLastError();
+  return launch_pdl(k_commit, dim3(1), dim3(kCommitThreads), 0, stream, out, cp);
 }
 
 }  // namespace sv

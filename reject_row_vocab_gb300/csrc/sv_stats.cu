@@ -5,20 +5,26 @@
 // Z = sum_v 2^((l_v - M) * log2(e)/T), the normaliser of softmax(l/T)
 // ([E2D] §6.2).  [E2D] = "从 EAGLE 到 DFlash 2：SGLang 与 SpecForge 的投机解码训练和推理".
 //
-// Work split: the rows are viewed as one flat sequence of 16-byte vectors and
-// the grid (one resident wave) takes equal contiguous ranges of it, so every
-// CTA streams the same number of bytes whatever the row count.  A row cut by
-// range boundaries is finished by the last CTA that touches it: each CTA
-// publishes its partial (m, s, argmax) for the cut rows, takes a ticket on the
-// row's counter, and the CTA drawing the final ticket merges the partials in
-// CTA order (deterministic) and resets the counter.  No CTA waits on another.
-//
-// Data movement: one producer warp streams the CTA's range into a ring of
-// shared-memory stages with bulk copies (the TMA engine, completion counted on
-// an mbarrier per stage); eight consumer warps fold each stage and release it.
-// Bytes in flight per SM are set by the ring, not by registers.  Every wait is
-// bounded (one second); a timeout raises the workspace error word, which the
-// acceptance kernels report as SV_DEV_TIMEOUT.
+// Work split: rows are cut into stages of 1024 16-byte vectors (16 KB) and
+// stages into chunks, the unit of scheduling and of partial results.  Most
+// rows use chunks of up to eight stages; the last rows, about three chunks'
+// worth per CTA, use one-stage chunks, so CTAs that run out of work at
+// different times are evened out by small pieces (the layout depends only on
+// the shapes and the grid).  One resident wave of CTAs takes chunks from a
+// queue: a CTA's first chunk is its own index, later ones come from an atomic
+// counter, requested two chunks ahead.  Per CTA, a producer warp streams
+// stages into a four-stage shared-memory ring with bulk copies (the TMA
+// engine; completion counted on an mbarrier per stage), eight consumer warps
+// fold each stage with packed fp32x2 arithmetic against an exponent reference
+// that moves only when a logit grows 16 log2 units past it, and at the end of
+// a chunk each warp combines its lanes and hands the result to a finalizer
+// warp, which writes the chunk's partial (maximum, the first vector holding
+// it, the sum rescaled to the maximum, flags).  k_row_merge then merges each
+// row's chunk partials in chunk order, so the result does not depend on which
+// CTA streamed what, and finds the argmax element in the one vector the merge
+// points to.  No CTA waits on another.  Every mbarrier wait is bounded (one
+// second); a timeout raises the workspace error word, reported by the next
+// kernels as SV_DEV_TIMEOUT.
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -28,31 +34,89 @@ namespace sv {
 namespace {
 
 constexpr int kConsumers = 256;                      // eight consumer warps
-constexpr int kProducerWarp = kConsumers / 32;       // warp 8 streams the stages
-constexpr int kFinalizerWarp = kProducerWarp + 1;    // warp 9 finishes each row
+constexpr int kConsumerWarps = kConsumers / 32;
+constexpr int kProducerWarp = kConsumerWarps;        // warp 8 streams the stages
+constexpr int kFinalizerWarp = kProducerWarp + 1;    // warp 9 merges partials
 constexpr int kStatsThreads = kConsumers + 64;
 constexpr int kChunkVecs = 1024;                     // 16 KB per stage
 constexpr int kStages = 4;
+constexpr int kHeadChunkStages = 8;                  // chunks of the head rows span up to eight stages
+constexpr int kTailRounds = 3;                       // tail rows hold about this many one-stage chunks per CTA
+constexpr int kSlots = 4;                            // chunk partials in flight to the finalizer
+constexpr int kTabCap = 512;                         // request tables staged in shared memory up to this size
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-constexpr int kRowsCached = 64;  // per-row log2(e)/T precomputed for the first rows of a range
+constexpr uint32_t kProducerNap = 32;   // ns between polls: the producer's reaction time matters
+constexpr uint32_t kConsumerNap = 128;  // consumers and finalizer mostly wait for memory
 
-// One consumer thread's statistics for one row segment, handed to the finalizer.
-struct SegSlot {
-  float m;
-  float s;        // sum of 2^((l - m) k)
-  int32_t vidx;   // vector holding the first occurrence of m (to resolve), or -1
-  int32_t idx;    // resolved index when vidx < 0
-  uint32_t flags;
+// What the producer tells the consumers about one stage.
+struct StageMeta {
+  int32_t item;  // chunk index in the queue, -1 marks the end
+  int32_t row;
+  int32_t c0;    // first vector of the stage within the row
+  int32_t n;     // full vectors in the stage
+  float k;       // log2(e)/T of the row (0: greedy row, no sums)
+  float ik;      // 1/k (0 for greedy rows)
+  int32_t nst;   // stages in this chunk
+  int32_t tail;  // 1: the row's ragged tail vector follows this chunk
+};
+
+// How rows are cut into chunks (queue items).  Head rows [0, rows_a) are cut
+// into cpr_a nearly equal chunks of up to kHeadChunkStages stages (few queue
+// and bookkeeping operations per byte); the remaining tail rows into one-stage
+// chunks (fine-grained work for the end of the pass, when CTAs run out of
+// queue at different times).  Items are numbered head rows first, so the
+// queue hands out the coarse work first.  The layout depends only on the
+// shapes and the grid, so the merge order of every row is fixed.
+struct ChunkPlan {
+  int32_t nst;     // stages (1024-vector pieces) per row, at least 1
+  int32_t cpr_a;   // chunks per head row
+  int32_t rows_a;  // head rows
+  int32_t cpr_b;   // chunks per tail row (= nst)
+  int64_t n_a;     // items in the head rows
+  int64_t n_items;
+};
+
+// Row, stage range [s0, s1) and "last chunk of its row" of a queue item.
+__device__ __forceinline__ void chunk_geometry(const ChunkPlan& P, int32_t item, int32_t& row, int32_t& s0,
+                                               int32_t& s1, bool& last) {
+  if (item < P.n_a) {
+    row = item / P.cpr_a;
+    const int32_t ci = item - row * P.cpr_a;
+    s0 = ci * P.nst / P.cpr_a;
+    s1 = (ci + 1) * P.nst / P.cpr_a;
+    last = ci == P.cpr_a - 1;
+  } else {
+    const int32_t j = item - static_cast<int32_t>(P.n_a);
+    const int32_t r = j / P.cpr_b;
+    const int32_t ci = j - r * P.cpr_b;
+    row = P.rows_a + r;
+    s0 = ci;
+    s1 = ci + 1;
+    last = ci == P.cpr_b - 1;
+  }
+}
+
+// One chunk's per-warp partials, handed from the consumers to the finalizer.
+struct ChunkSlot {
+  Part wpart[kConsumerWarps];
+  int32_t item;
+  int32_t row;
+  float k;
+  int32_t pad;
 };
 
 struct StatsSmem {
   uint4 buf[kStages][kChunkVecs];
-  SegSlot seg[2][kConsumers];
-  unsigned long long full[kStages];
-  unsigned long long empty[kStages];
-  unsigned long long seg_full[2];
-  unsigned long long seg_empty[2];
-  float kc[kRowsCached];
+  StageMeta meta[kStages];
+  ChunkSlot slot[kSlots];
+  float tab_k[kTabCap];    // log2(e)/T by request (or by row)
+  float tab_ik[kTabCap];   // T/log2(e), the reciprocal of tab_k (0 for greedy rows)
+  int32_t tab_cu[kTabCap]; // request offsets of a ragged layout
+  unsigned long long tab_ready;
+  unsigned long long full[kStages];    // producer -> consumers (bulk-copy bytes)
+  unsigned long long empty[kStages];   // consumers -> producer
+  unsigned long long pfull[kSlots];    // consumers -> finalizer
+  unsigned long long pempty[kSlots];   // finalizer -> consumers
   int abort;
 };
 constexpr size_t kStatsSmemBytes = sizeof(StatsSmem) + 128;  // + alignment slack
@@ -70,32 +134,66 @@ struct VecTraits<SV_F32> {
   static constexpr int ES = 4;
 };
 
-// Per-thread running statistics: maximum m, the vector where m was last
-// raised (its element index is resolved once, at the end of the range), the
-// resolved argmax, flags, and a packed fp32 accumulator of 2^((l - r) k)
-// against a reference r that trails m: r only moves when m outgrows it by
-// more than kRefSlack (in log2 units), so most vectors need no rescale.
+// Per-thread running statistics of one chunk: the maximum m, the first vector
+// (within the row) where it was reached (its element is found once per row,
+// at the end), flags, and a packed fp32 accumulator of 2^(l k - R) against a
+// reference R in log2 units.  R only moves when a logit reaches `bound`
+// (about R + 16 log2 units), so most vectors need no rescale and every term is
+// one fused multiply-add and one exponential.
 struct ThreadAcc {
   float m;
-  int32_t vidx;  // vector (within the row) holding the first occurrence of m, -1 if none yet
-  int32_t idx;   // resolved argmax (tail handling and after resolution)
+  int32_t vidx;  // -1 while no usable entry has been seen
   uint32_t flags;
-  float r;       // exponent reference, starts at -FLT_MAX (finite: no inf - inf)
+  float R;
+  float bound;   // logits >= bound move the reference (+inf for greedy rows)
   float2 s;
 };
 
 constexpr float kRefSlack = 16.0f;  // terms stay <= 2^16 between reference moves
 constexpr float kMinFinite = -3.402823466e38f;
 
+template <bool EXP>
 __device__ __forceinline__ ThreadAcc acc_init() {
-  return ThreadAcc{-kInfF, -1, -1, 0u, kMinFinite, make_float2(0.0f, 0.0f)};
+  return ThreadAcc{-kInfF, -1, 0u, 0.0f, EXP ? kMinFinite : kInfF, make_float2(0.0f, 0.0f)};
 }
 
-// The accumulated sum expressed against the maximum m (for merging).
-__device__ __forceinline__ float acc_sum_at_max(const ThreadAcc& a, float k) {
-  const float s = a.s.x + a.s.y;
-  if (s == 0.0f || a.r == a.m) return s;
-  return s * exp2f((a.r - a.m) * k);
+// Move the reference up to the finite logit v (rare path).
+__device__ __forceinline__ void move_ref(ThreadAcc& a, float v, float k, float ik) {
+  const float Rn = v * k;
+  if (!(fabsf(Rn) < kInfF)) {  // l * log2(e)/T outside fp32: no meaningful sum
+    a.flags |= kStNonFinite;
+    a.bound = kInfF;
+    return;
+  }
+  const bool have = a.s.x != 0.0f || a.s.y != 0.0f;
+  const float f = have ? exp2f(a.R - Rn) : 0.0f;
+  a.s = __fmul2_rn(a.s, make_float2(f, f));
+  a.R = Rn;
+  a.bound = (Rn + kRefSlack) * ik;
+}
+
+// Order-preserving map of a float (never NaN here) to an unsigned key.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+__device__ __forceinline__ float warp_max(float m) {
+  return key_float(__reduce_max_sync(0xffffffffu, order_key(m)));
+}
+
+// Combine one partial per lane into the warp's, given the warp maximum M and
+// each lane's log2 factor e that rescales its sum s to M: the sum of the
+// rescaled sums (the butterfly leaves the same value in every lane), the
+// lowest vector holding M, and the union of the flags.
+__device__ __forceinline__ Part warp_combine(float M, float m, float s, float e, int32_t vidx, uint32_t flags) {
+  float sc = s != 0.0f ? (e == 0.0f ? s : s * exp2f(e)) : 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+  const int32_t V = __reduce_min_sync(0xffffffffu, (m == M && vidx >= 0) ? vidx : INT32_MAX);
+  return Part{M, sc, V == INT32_MAX ? -1 : V, __reduce_or_sync(0xffffffffu, flags)};
 }
 
 template <int DT>
@@ -130,14 +228,14 @@ __device__ __forceinline__ float raw_max_nan(const uint4& raw) {
   }
 }
 
-// Sum of 2^((x - m) k) over E elements, as a packed pair (fixed order).
+// Sum of 2^(x k - R) over E elements, as a packed pair (fixed order).
 template <int E>
-__device__ __forceinline__ float2 exp_sum(const float (&x)[E], float m, float k) {
-  const float2 nm = make_float2(-m, -m), kk = make_float2(k, k);
+__device__ __forceinline__ float2 exp_sum(const float (&x)[E], float k, float R) {
+  const float2 kk = make_float2(k, k), nR = make_float2(-R, -R);
   float2 e[E / 2];
 #pragma unroll
   for (int i = 0; i < E / 2; ++i) {
-    const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[2 * i], x[2 * i + 1]), nm), kk);
+    const float2 t = __ffma2_rn(make_float2(x[2 * i], x[2 * i + 1]), kk, nR);
     e[i] = make_float2(ex2_fast(t.x), ex2_fast(t.y));
   }
   if constexpr (E == 8) {
@@ -148,333 +246,528 @@ __device__ __forceinline__ float2 exp_sum(const float (&x)[E], float m, float k)
 }
 
 // Fold E logits one at a time, NaN and +inf entries read as -inf (the caller
-// flags them).  immediate: record the argmax index itself, else the vector.
+// flags them).
 template <int E, bool EXP>
-__device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E], int32_t vec, float k,
-                                              bool immediate) {
+__device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E], int32_t vec, float k, float ik) {
   for (int i = 0; i < E; ++i) {
     const float v = usable_logit(x[i]) ? x[i] : -kInfF;
     if (v > a.m) {
       a.m = v;
-      if (immediate) {
-        a.idx = vec * E + i;
-        a.vidx = -1;  // the pending vector no longer holds the maximum
-      } else {
-        a.vidx = vec;
-      }
+      a.vidx = vec;
     }
     if (EXP) {
-      if (v > a.r) {  // exact reference moves here (rare path)
-        const float f = a.r > kMinFinite ? exp2f((a.r - v) * k) : 0.0f;
-        a.s = __fmul2_rn(a.s, make_float2(f, f));
-        a.r = v;
-      }
-      a.s.x += ex2_fast((v - a.r) * k);
+      if (v >= a.bound) move_ref(a, v, k, ik);
+      a.s.x += ex2_fast(fmaf(v, k, -a.R));
     }
   }
 }
 
-// Fold one vector.  The common case (clean data, maximum within the slack of
-// the reference) is branch-free.
+// Fold one vector.  The common case (clean data, maximum below the bound) is
+// branch-free.
 template <int DT, bool EXP>
-__device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float slack) {
+__device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
   float x[E];
   unpack<DT>(raw, x);
   const float vmax = raw_max_nan<DT>(raw);
-  const float bound = EXP ? a.r + slack : kInfF;
-  if (!(vmax < bound)) {  // NaN / +inf present, or the maximum outgrew the reference (rare)
+  if (!(vmax < a.bound)) {  // NaN / +inf present, or the reference must move (rare)
     if (!(vmax < kInfF)) {
       a.flags |= kStNonFinite;
-      consume_dirty<E, EXP>(a, x, vec, k, false);
+      consume_dirty<E, EXP>(a, x, vec, k, ik);
       return;
     }
-    if (EXP) {
-      const float f = a.r > kMinFinite ? exp2f((a.r - vmax) * k) : 0.0f;
-      a.s = __fmul2_rn(a.s, make_float2(f, f));
-      a.r = vmax;
-    }
+    if (EXP) move_ref(a, vmax, k, ik);
   }
   const bool raised = vmax > a.m;
   a.vidx = raised ? vec : a.vidx;
   a.m = fmaxf(a.m, vmax);
-  if (EXP) a.s = __fadd2_rn(a.s, exp_sum<E>(x, a.r, k));
+  if (EXP) a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
 }
 
-// The index of the first entry equal to m in vector vidx of a row.
-template <int DT>
-__device__ __forceinline__ int32_t resolve_index(const char* rowp, int32_t vidx, float m) {
-  constexpr int E = VecTraits<DT>::E;
-  float x[E];
-  unpack<DT>(ld_stream16(rowp + static_cast<int64_t>(vidx) * 16), x);
-  int j = E - 1;
-#pragma unroll
-  for (int i = E - 1; i >= 0; --i)
-    if (x[i] == m) j = i;
-  return vidx * E + j;
-}
-
-// The row's ragged tail vector (vocab not a multiple of the vector width), by one thread.
+// The row's ragged tail (vocab not a multiple of the vector width) as vector nfull, by one thread.
 template <int DT, bool EXP>
-__device__ __forceinline__ void fold_tail(ThreadAcc& a, const LogitsView& lg, int64_t row, int64_t nfull, float k) {
+__device__ __forceinline__ void fold_tail(ThreadAcc& a, const LogitsView& lg, int64_t row, int64_t nfull, float k,
+                                          float ik) {
   constexpr int E = VecTraits<DT>::E;
   float x[E];
 #pragma unroll
   for (int i = 0; i < E; ++i) {
     const int64_t col = nfull * E + i;
     x[i] = col < lg.vocab ? load_logit(lg, row, col) : -kInfF;
-    if (!usable_logit(x[i])) a.flags |= kStNonFinite;
+    if (col < lg.vocab && !usable_logit(x[i])) a.flags |= kStNonFinite;
   }
-  consume_dirty<E, EXP>(a, x, static_cast<int32_t>(nfull), k, true);
+  consume_dirty<E, EXP>(a, x, static_cast<int32_t>(nfull), k, ik);
 }
 
-// Fold the first n vectors of a stage (chunk starting at vector c0 of the row).
+// Fold the first n vectors of a stage (vectors c0.. of the row).  A full
+// stage takes the thread's four vectors together: one check of their maximum
+// against the bound covers all four, then maxima and sums run branch-free.
 template <int DT, bool EXP>
-__device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k,
-                                           float slack) {
+__device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k, float ik) {
+  constexpr int E = VecTraits<DT>::E;
   constexpr int PER = kChunkVecs / kConsumers;  // vectors per consumer thread per full stage
   const int t = threadIdx.x;
   if (n == kChunkVecs) {
     uint4 raw[PER];
+    float vm[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) raw[j] = lds16(stage_addr + (t + j * kConsumers) * 16);
 #pragma unroll
-    for (int j = 0; j < PER; ++j) consume<DT, EXP>(a, raw[j], c0 + t + j * kConsumers, k, slack);
+    for (int j = 0; j < PER; ++j) vm[j] = raw_max_nan<DT>(raw[j]);
+    float smax = vm[0];
+#pragma unroll
+    for (int j = 1; j < PER; ++j) smax = fmax_nan(smax, vm[j]);
+    if (!(smax < a.bound)) {  // NaN / +inf, or the reference must move: vector by vector (rare)
+#pragma unroll
+      for (int j = 0; j < PER; ++j) consume<DT, EXP>(a, raw[j], c0 + t + j * kConsumers, k, ik);
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      a.vidx = vm[j] > a.m ? c0 + t + j * kConsumers : a.vidx;
+      a.m = fmaxf(a.m, vm[j]);
+    }
+    if (EXP) {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        float x[E];
+        unpack<DT>(raw[j], x);
+        a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
+      }
+    }
   } else {
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
       const int vi = t + j * kConsumers;
-      if (vi < n) consume<DT, EXP>(a, lds16(stage_addr + vi * 16), c0 + vi, k, slack);
+      if (vi < n) consume<DT, EXP>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik);
     }
   }
 }
 
-__device__ __forceinline__ float row_k(const RowMap& map, int64_t row) {
-  float T = 0.0f;
+// The index of the first entry equal to M in vector vidx of a row (the ragged
+// tail when vidx == nfull), read back from global memory once per row.
+template <int DT>
+__device__ __forceinline__ int32_t resolve_index(const LogitsView& lg, int64_t row, int64_t nfull, int32_t vidx,
+                                                 float M) {
+  constexpr int E = VecTraits<DT>::E;
+  if (vidx < 0) return -1;
+  float x[E];
+  if (vidx < nfull) {
+    const uint4 raw = ld_stream16(reinterpret_cast<const uint4*>(static_cast<const char*>(lg.base) +
+                                                                 row * lg.ld * VecTraits<DT>::ES) +
+                                  vidx);
+    unpack<DT>(raw, x);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int64_t col = static_cast<int64_t>(vidx) * E + i;
+      x[i] = col < lg.vocab ? load_logit(lg, row, col) : -kInfF;
+    }
+  }
+  int j = E - 1;
+#pragma unroll
+  for (int i = E - 1; i >= 0; --i)
+    if (x[i] == M) j = i;
+  return vidx * E + j;
+}
+
+// Size of the request table a row map needs (temperatures, or offsets for a
+// ragged layout), 0 for greedy rows.
+__device__ __forceinline__ int32_t map_table_size(const RowMap& map, int64_t rows) {
   switch (map.kind) {
     case kMapFixed:
-      T = map.temperature[row / map.rows_per_req];
-      break;
-    case kMapCu: {
-      int lo = 0, hi = map.batch - 1;
-      while (lo < hi) {  // last request whose start is <= row
-        const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int64_t>(map.cu[mid]) <= row) {
-          lo = mid;
-        } else {
-          hi = mid - 1;
-        }
-      }
-      T = map.temperature[lo];
-      break;
-    }
+      return map.batch;
+    case kMapCu:
+      return map.batch + 1;
     case kMapPerRow:
-      T = map.temperature[row];
-      break;
+      return rows > kTabCap ? kTabCap + 1 : static_cast<int32_t>(rows);
     default:
-      T = 0.0f;
+      return 0;
   }
-  return temperature_k(T);
 }
 
-__device__ __forceinline__ int64_t cta_of_vector(int64_t v, int64_t G, int64_t NV) {
-  return ((v + 1) * G - 1) / NV;
+// Index of a row's entry in the request tables (request, or the row itself
+// for per-row temperatures), computed by a whole warp (same value in every
+// lane).  Ragged layouts search the request offsets 32 at a time, so a lookup
+// costs one round trip per factor of 32 in the batch size.
+__device__ __forceinline__ int32_t row_entry(const RowMap& map, int32_t row, int lane, const int32_t* cu) {
+  switch (map.kind) {
+    case kMapFixed:
+      return row / map.rows_per_req;
+    case kMapPerRow:
+      return row;
+    case kMapCu: {
+      // Invariant: cu[lo] <= row (cu[0] = 0); the answer, the last request
+      // starting at or before row, is in [lo, hi].
+      int32_t lo = 0, hi = map.batch - 1;
+      while (hi > lo) {
+        const int32_t step = (hi - lo + 31) / 32;
+        const int32_t j = lo + (lane + 1) * step;
+        const bool le = j <= hi && cu[j] <= row;
+        const int32_t c = __popc(__ballot_sync(0xffffffffu, le));  // offsets are sorted: a prefix of lanes
+        hi = min(hi, lo + (c + 1) * step - 1);
+        lo += c * step;
+      }
+      return lo;
+    }
+    default:
+      return -1;  // greedy rows
+  }
 }
 
-// The row's final statistics from its merged partial.
-__device__ __forceinline__ RowStat finish_row(const Part& p, float k) {
-  RowStat st;
-  const bool samp = k > 0.0f && p.m > -kInfF;
-  st.Z = samp ? p.s : 0.0f;
-  st.inv_z = samp ? __fdiv_rn(1.0f, p.s) : 0.0f;
-  st.M = p.m;
-  st.argmax = p.idx;
-  st.flags = p.flags;
-  st.k = k;
-  return st;
+// Temperature of a row read from global memory (whole warp).
+__device__ __forceinline__ float row_temperature(const RowMap& map, int32_t row, int lane) {
+  const int32_t e = row_entry(map, row, lane, map.cu);
+  return e < 0 ? 0.0f : map.temperature[e];
 }
 
-// Segment geometry of one row within a CTA's range.
-struct Seg {
-  int64_t s0, s1, sf;  // vectors [s0, s1) of the row are ours; [s0, sf) are full vectors
-};
-
-__device__ __forceinline__ Seg segment_of(int64_t row, int64_t NVr, int64_t v_begin, int64_t v_end, int64_t nfull) {
-  const int64_t row_v0 = row * NVr;
-  Seg g;
-  g.s0 = (v_begin > row_v0 ? v_begin : row_v0) - row_v0;
-  g.s1 = (v_end < row_v0 + NVr ? v_end : row_v0 + NVr) - row_v0;
-  g.sf = g.s1 < nfull ? g.s1 : nfull;
-  return g;
+// Merge chunk partial b into a (sums relative to each side's own maximum).
+__device__ __forceinline__ void chunk_merge(Part& a, const Part& b, float k) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -kInfF) {
+    a.flags |= b.flags;
+    return;
+  }
+  const float sa = a.s != 0.0f && a.m != M ? a.s * exp2f((a.m - M) * k) : a.s;
+  const float sb = b.s != 0.0f && b.m != M ? b.s * exp2f((b.m - M) * k) : b.s;
+  int32_t v = -1;
+  if (a.m == M && a.idx >= 0) v = a.idx;
+  if (b.m == M && b.idx >= 0 && (v < 0 || b.idx < v)) v = b.idx;
+  a = Part{M, sa + sb, v, a.flags | b.flags};
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, int64_t NVr,
-                                                                int64_t NV) {
+__global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan) {
   using VT = VecTraits<DT>;
   constexpr int E = VT::E;
+  const int64_t n_items = plan.n_items;
   extern __shared__ unsigned char smem_raw[];
   StatsSmem& sm = *reinterpret_cast<StatsSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  const int64_t G = gridDim.x, c = blockIdx.x;
-  const int64_t v_begin = c * NV / G, v_end = (c + 1) * NV / G;
-  if (v_begin >= v_end) return;
-  const int64_t r_first = v_begin / NVr, r_last = (v_end - 1) / NVr;
   const int64_t nfull = lg.vocab / E;
+  const bool ragged = nfull * E < lg.vocab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned* queue = ws.done_cnt + 2;
+  volatile int* abort = &sm.abort;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_addr(&sm.full[s]), 1);
-      mbar_init(smem_addr(&sm.empty[s]), kConsumers / 32);
+      mbar_init(smem_addr(&sm.empty[s]), kConsumerWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&sm.seg_full[s]), kConsumers);
-      mbar_init(smem_addr(&sm.seg_empty[s]), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_addr(&sm.pfull[s]), kConsumerWarps);
+      mbar_init(smem_addr(&sm.pempty[s]), 1);
     }
+    mbar_init(smem_addr(&sm.tab_ready), 1);
     sm.abort = 0;
     mbar_fence_init();
   }
-  // the temperatures of the first rows, fetched once while the first stages load
-  if (threadIdx.x < kRowsCached && r_first + threadIdx.x <= r_last) sm.kc[threadIdx.x] = row_k(map, r_first + threadIdx.x);
   __syncthreads();
+  grid_dependency_wait();  // the logits may come from the previous kernel on the stream
+  allow_dependents();
 
+  const int32_t tab_n = map_table_size(map, lg.rows);
+  const bool tabbed = tab_n > 0 && tab_n <= kTabCap;
   if (warp == kProducerWarp) {  // ------------------------------------------ producer
+    // The whole warp walks the queue; lane 0 drives the ring.  A CTA's first
+    // chunk is its own index, later ones gridDim.x + a ticket.  Two tickets are kept in flight in two
+    // different registers (a register is busy for the whole warp while any
+    // atomic writes it), so each ticket is read two chunks after it was
+    // requested.  A stage's
+    // copy is issued before the row's temperature is first used: the full
+    // barrier completes only after the stage description is written and
+    // arrived on.
+    uint32_t g = 0;  // stages issued
+    unsigned tka = 0, tkb = 0;
     if (lane == 0) {
-      uint32_t g = 0;
-      for (int64_t row = r_first; row <= r_last && !sm.abort; ++row) {
-        const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
-        const char* rowp = static_cast<const char*>(lg.base) + row * lg.ld * VT::ES;
-        for (int64_t c0 = sg.s0; c0 < sg.sf; c0 += kChunkVecs, ++g) {
-          const int n = static_cast<int>(sg.sf - c0 < kChunkVecs ? sg.sf - c0 : kChunkVecs);
-          const int st = g % kStages;
-          if (!mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
-            sm.abort = 1;
-            atomicOr(ws.err, 1u);
-            break;
+      tka = atomicAdd(queue, 1u);
+      tkb = atomicAdd(queue, 1u);
+    }
+    int64_t pos = blockIdx.x;
+    // k and 1/k of a row: from the staged tables, else computed from a global read.
+    auto row_k_of = [&](int32_t row, float& k, float& ik) {
+      if (tabbed) {
+        const int32_t e = row_entry(map, row, lane, sm.tab_cu);
+        k = e < 0 ? 0.0f : sm.tab_k[e];
+        ik = e < 0 ? 0.0f : sm.tab_ik[e];
+      } else {
+        k = temperature_k(row_temperature(map, row, lane));
+        ik = k > 0.0f ? __frcp_rn(k) : 0.0f;
+      }
+    };
+    float nk = 0.0f, nik = 0.0f;  // k and 1/k of the next chunk's row
+    bool have_k = false, ok = true;
+    // Stream the chunk at queue position `pos`, then move to the position whose ticket is in `tk`.
+    auto chunk_out = [&](unsigned& tk) {
+      const int32_t item = static_cast<int32_t>(pos);
+      int32_t row, s0, s1;
+      bool last;
+      chunk_geometry(plan, item, row, s0, s1, last);
+      const int32_t cc0 = s0 * kChunkVecs;
+      const int64_t left = nfull - cc0;
+      const int32_t span = (s1 - s0) * kChunkVecs;
+      const int32_t cn = left <= 0 ? 0 : static_cast<int32_t>(left < span ? left : span);
+      const int32_t nst = s1 - s0;
+      const int32_t tail = (ragged && last) ? 1 : 0;
+      float k = 0.0f, ik = 0.0f;
+      for (int32_t s = 0; s < nst; ++s, ++g) {
+        const int st = g % kStages;
+        const int32_t c0 = cc0 + s * kChunkVecs;
+        const int32_t rem = cn - s * kChunkVecs;
+        const int32_t n = rem <= 0 ? 0 : (rem < kChunkVecs ? rem : kChunkVecs);
+        if (lane == 0) {
+          ok = mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs,
+                                 kProducerNap);
+          if (ok && n > 0) {
+            mbar_expect_tx(smem_addr(&sm.full[st]), n * 16);
+            bulk_copy_g2s(smem_addr(&sm.buf[st][0]),
+                          static_cast<const char*>(lg.base) + (row * lg.ld * VT::ES) + int64_t{c0} * 16, n * 16,
+                          smem_addr(&sm.full[st]));
           }
-          mbar_arrive_expect_tx(smem_addr(&sm.full[st]), n * 16);
-          bulk_copy_g2s(smem_addr(&sm.buf[st][0]), rowp + c0 * 16, n * 16, smem_addr(&sm.full[st]));
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) return;
+        if (s == 0) {
+          if (!have_k) {  // the first chunk: wait for the staged tables
+            if (tabbed && lane == 0) {
+              volatile int never = 0;
+              ok = mbar_wait_bounded(smem_addr(&sm.tab_ready), 0u, &never, kWaitLimitNs);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return;
+            row_k_of(row, nk, nik);
+            have_k = true;
+          }
+          k = nk;  // first use of the prefetched values: after the copy is on its way
+          ik = nik;
+          asm volatile("mov.b32 %0, %0;" : "+f"(k));
+        }
+        if (lane == 0) {
+          sm.meta[st] = StageMeta{item, row, c0, n, k, ik, nst, tail};
+          mbar_arrive(smem_addr(&sm.full[st]));
         }
       }
-      for (int s = 0; s < kStages && g > 0; ++s) {  // drain before the CTA may exit
-        --g;
-        volatile int never = 0;
-        mbar_wait_bounded(smem_addr(&sm.full[g % kStages]), (g / kStages) & 1u, &never, kWaitLimitNs);
+      pos = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, tk, 0);
+      if (lane == 0 && pos < n_items) tk = atomicAdd(queue, 1u);
+      if (pos < n_items) {
+        int32_t nrow, ns0, ns1;
+        bool nlast;
+        chunk_geometry(plan, static_cast<int32_t>(pos), nrow, ns0, ns1, nlast);
+        row_k_of(nrow, nk, nik);
+      }
+    };
+    while (pos < n_items) {
+      chunk_out(tka);
+      if (!ok || pos >= n_items) break;
+      chunk_out(tkb);
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      bool ended = false;
+      if (!ok) {
+        sm.abort = 1;
+        atomicOr(ws.err, 1u);
+      } else if (!*abort) {  // end marker
+        const int st = g % kStages;
+        if (mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
+          sm.meta[st] = StageMeta{-1, 0, 0, 0, 0.0f, 0.0f, 0, 0};
+          mbar_arrive(smem_addr(&sm.full[st]));
+          ended = true;
+        } else {
+          sm.abort = 1;
+          atomicOr(ws.err, 1u);
+        }
+      }
+      if (*abort) {
+        // The consumers may have left with copies still in flight: wait for the
+        // last copy on each stage before the CTA exits.  Copies older than the
+        // last kStages stages, and the stage the end marker reused, were
+        // consumed before the producer could move on.
+        const uint32_t first = g >= kStages ? g - kStages + (ended ? 1u : 0u) : 0u;
+        for (uint32_t i = first; i < g; ++i) {
+          volatile int never = 0;
+          if (!mbar_wait_bounded(smem_addr(&sm.full[i % kStages]), (i / kStages) & 1u, &never, kWaitLimitNs))
+            atomicOr(ws.err, 1u);
+        }
       }
     }
     return;
   }
 
   if (warp == kFinalizerWarp) {  // ---------------------------------------- finalizer
-    uint32_t i = 0;
-    for (int64_t row = r_first; row <= r_last; ++row, ++i) {
-      const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
-      const char* rowp = static_cast<const char*>(lg.base) + row * lg.ld * VT::ES;
-      const float k = row - r_first < kRowsCached ? sm.kc[row - r_first] : row_k(map, row);
-      const int slot = i & 1;
-      if (!mbar_wait_bounded(smem_addr(&sm.seg_full[slot]), (i >> 1) & 1u, &sm.abort, kWaitLimitNs)) {
+    if (tabbed) {  // stage the request tables: k = log2(e)/T and its reciprocal, per request
+      for (int32_t i0 = 0; i0 < tab_n; i0 += 32 * 8) {
+        float tv[8];
+        int32_t cv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {  // all loads first, then all stores: one round trip per 256 entries
+          const int32_t i = i0 + u * 32 + lane;
+          const bool in = i < tab_n;
+          const bool has_t = in && (map.kind != kMapCu || i < map.batch);
+          tv[u] = has_t ? map.temperature[i] : 0.0f;
+          cv[u] = (in && map.kind == kMapCu) ? map.cu[i] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int32_t i = i0 + u * 32 + lane;
+          if (i < tab_n) {
+            const float k = temperature_k(tv[u]);
+            sm.tab_k[i] = k;
+            sm.tab_ik[i] = k > 0.0f ? __frcp_rn(k) : 0.0f;
+            sm.tab_cu[i] = cv[u];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.tab_ready));
+    }
+    // Each chunk's partial goes to the workspace; k_row_merge combines them
+    // per row after this grid completes (no cross-CTA waiting here).
+    for (uint32_t c = 0;; ++c) {
+      const int sl = c % kSlots;
+      if (!mbar_wait_bounded(smem_addr(&sm.pfull[sl]), (c / kSlots) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
         sm.abort = 1;
         atomicOr(ws.err, 1u);
+        break;
       }
-      // each lane folds eight consumers' statistics, resolving argmax indices from the row
-      constexpr int PER = kConsumers / 32;
-      SegSlot sl[PER];
-#pragma unroll
-      for (int t = 0; t < PER; ++t) sl[t] = sm.seg[slot][lane * PER + t];
+      const int32_t item = sm.slot[sl].item;
+      const float k = sm.slot[sl].k;
+      Part wp = lane < kConsumerWarps ? sm.slot[sl].wpart[lane] : part_identity();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sm.seg_empty[slot]));  // the slot is free again
-      // Only the consumers holding the segment maximum need their index resolved.
-      float mseg = -kInfF;
-#pragma unroll
-      for (int t = 0; t < PER; ++t) mseg = fmaxf(mseg, sl[t].m);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) mseg = fmaxf(mseg, __shfl_xor_sync(0xffffffffu, mseg, off));
-      int32_t idx[PER];
-#pragma unroll
-      for (int t = 0; t < PER; ++t)
-        idx[t] = (sl[t].vidx >= 0 && sl[t].m == mseg) ? resolve_index<DT>(rowp, sl[t].vidx, sl[t].m) : sl[t].idx;
-      Part p = part_identity();
-#pragma unroll
-      for (int t = 0; t < PER; ++t) part_merge(p, Part{sl[t].m, sl[t].s, idx[t], sl[t].flags}, k);
-      p = part_warp_reduce(p, k);
-
-      const int64_t c_lo = cta_of_vector(row * NVr, G, NV);
-      const int64_t c_hi = cta_of_vector(row * NVr + NVr - 1, G, NV);
-      if (c_lo == c_hi) {  // the whole row is ours
-        if (lane == 0) ws.rowstat[row] = finish_row(p, k);
-        continue;
-      }
-      int last = 0;
-      if (lane == 0) {
-        RowPartial rp;
-        rp.s = p.s;
-        rp.m = p.m;
-        rp.idx = p.idx;
-        rp.flags = p.flags;
-        ws.partial[2 * c + (row == r_first ? 0 : 1)] = rp;
-        const unsigned ticket = ticket_add(&ws.row_cnt[row], 1u);
-        last = (ticket == static_cast<unsigned>(c_hi - c_lo));
-      }
-      if (__shfl_sync(0xffffffffu, last, 0)) {  // last arriver: merge the row's partials in CTA order
-        __syncwarp();
-        Part acc = part_identity();
-        for (int64_t cc = c_lo + lane; cc <= c_hi; cc += 32) {
-          const int64_t first_row_cc = (cc * NV / G) / NVr;
-          part_merge(acc, load_partial_cg(&ws.partial[2 * cc + (row == first_row_cc ? 0 : 1)]), k);
-        }
-        acc = part_warp_reduce(acc, k);
-        if (lane == 0) {
-          ws.rowstat[row] = finish_row(acc, k);
-          ws.row_cnt[row] = 0u;  // leave the counter clean for the next call
-        }
-      }
-      (void)sg;
+      if (lane == 0) mbar_arrive(smem_addr(&sm.pempty[sl]));  // the slot is free again
+      if (item < 0) break;
+      const float M = warp_max(wp.m);
+      wp = warp_combine(M, wp.m, wp.s, (wp.m - M) * k, wp.idx, wp.flags);
+      if (lane == 0) ws.partial[item] = RowPartial{wp.s, wp.m, wp.idx, wp.flags};
     }
     return;
   }
 
   // ---------------------------------------------------------------- consumers
-  uint32_t g = 0, i = 0;
-  for (int64_t row = r_first; row <= r_last; ++row, ++i) {
-    const Seg sg = segment_of(row, NVr, v_begin, v_end, nfull);
-    const float k = row - r_first < kRowsCached ? sm.kc[row - r_first] : row_k(map, row);
-    ThreadAcc a = acc_init();
-    const float slack = k > 0.0f ? kRefSlack / k : 0.0f;
-    for (int64_t c0 = sg.s0; c0 < sg.sf; c0 += kChunkVecs, ++g) {
-      const int n = static_cast<int>(sg.sf - c0 < kChunkVecs ? sg.sf - c0 : kChunkVecs);
-      const int st = g % kStages;
-      if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs)) {
-        sm.abort = 1;
-        atomicOr(ws.err, 1u);
-      } else if (k > 0.0f) {
-        fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), static_cast<int32_t>(c0), n, k, slack);
-      } else {
-        fold_stage<DT, false>(a, smem_addr(&sm.buf[st][0]), static_cast<int32_t>(c0), n, k, slack);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));
-    }
-    if (threadIdx.x == 0 && sg.s1 > nfull && nfull >= sg.s0) {  // the row's ragged tail vector
-      if (k > 0.0f) {
-        fold_tail<DT, true>(a, lg, row, nfull, k);
-      } else {
-        fold_tail<DT, false>(a, lg, row, nfull, k);
-      }
-    }
-    // hand the statistics to the finalizer and go on with the next row
-    const int slot = i & 1;
-    if (!mbar_wait_bounded(smem_addr(&sm.seg_empty[slot]), ((i >> 1) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
+  // Hand a chunk's warp partial (or the end mark, item < 0) to the finalizer.
+  auto hand_over = [&](uint32_t c, const Part& p, int32_t item, int32_t row, float k) -> bool {
+    const int sl = c % kSlots;
+    if (!mbar_wait_bounded(smem_addr(&sm.pempty[sl]), ((c / kSlots) & 1u) ^ 1u, &sm.abort, kWaitLimitNs,
+                           kConsumerNap)) {
       sm.abort = 1;
       atomicOr(ws.err, 1u);
+      return false;
     }
-    sm.seg[slot][threadIdx.x] = SegSlot{a.m, k > 0.0f ? acc_sum_at_max(a, k) : 0.0f, a.vidx, a.idx, a.flags};
-    mbar_arrive(smem_addr(&sm.seg_full[slot]));
+    if (lane == 0) {
+      sm.slot[sl].wpart[warp] = p;
+      if (warp == 0) {
+        sm.slot[sl].item = item;
+        sm.slot[sl].row = row;
+        sm.slot[sl].k = k;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&sm.pfull[sl]));
+    return true;
+  };
+  uint32_t g = 0;  // stages consumed
+  for (uint32_t c = 0;; ++c) {
+    int st = g % kStages;
+    if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+      sm.abort = 1;
+      atomicOr(ws.err, 1u);
+      break;
+    }
+    StageMeta md = sm.meta[st];
+    if (md.item < 0) {
+      hand_over(c, part_identity(), -1, 0, 0.0f);
+      break;
+    }
+    const int32_t item = md.item, row = md.row, nst = md.nst, tail = md.tail;
+    const float k = md.k, ik = md.ik;
+    Part p;
+    bool ok = true;
+    if (k > 0.0f) {
+      ThreadAcc a = acc_init<true>();  // one partial per chunk: independent of the schedule
+      for (int32_t s = 0;; ++s) {
+        fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));  // the stage goes back to the producer
+        ++g;
+        if (s + 1 == nst) break;
+        st = g % kStages;
+        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+          ok = false;
+          break;
+        }
+        md = sm.meta[st];
+      }
+      if (tail && threadIdx.x == 0) fold_tail<DT, true>(a, lg, row, nfull, k, ik);
+      const float M = warp_max(a.m);
+      // 2^(R - M k) rescales the lane's sum to the warp maximum (one rounding).
+      p = warp_combine(M, a.m, a.s.x + a.s.y, -fmaf(M, k, -a.R), a.vidx, a.flags);
+    } else {
+      ThreadAcc a = acc_init<false>();
+      for (int32_t s = 0;; ++s) {
+        fold_stage<DT, false>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, 0.0f, 0.0f);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));
+        ++g;
+        if (s + 1 == nst) break;
+        st = g % kStages;
+        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+          ok = false;
+          break;
+        }
+        md = sm.meta[st];
+      }
+      if (tail && threadIdx.x == 0) fold_tail<DT, false>(a, lg, row, nfull, 0.0f, 0.0f);
+      const float M = warp_max(a.m);
+      p = warp_combine(M, a.m, 0.0f, 0.0f, a.vidx, a.flags);
+    }
+    if (!ok) {
+      sm.abort = 1;
+      atomicOr(ws.err, 1u);
+      break;
+    }
+    if (!hand_over(c, p, item, row, k)) break;
+  }
+}
+
+// Row statistics from the chunk partials, one warp per row: merge the row's
+// chunks in chunk order (lane l takes chunks l, l+32, ...; the result does not
+// depend on which CTA streamed which chunk), find the argmax element in the
+// one vector the merge points to, and rewind the chunk queue for the next call.
+template <int DT>
+__global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan) {
+  grid_dependency_wait();  // the partials come from k_row_stats
+  allow_dependents();
+  if (blockIdx.x == 0 && threadIdx.x == 0) ws.done_cnt[2] = 0u;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x * int64_t{8} + (threadIdx.x >> 5);
+  if (row >= lg.rows) return;  // whole warps leave together
+  const int64_t nfull = lg.vocab / VecTraits<DT>::E;
+  // Same k as the streaming pass used: the same map, the same function.
+  const float k = temperature_k(row_temperature(map, static_cast<int32_t>(row), lane));
+  Part acc = part_identity();
+  const bool head = row < plan.rows_a;
+  const int32_t cnt = head ? plan.cpr_a : plan.cpr_b;
+  const int64_t base = head ? row * plan.cpr_a : plan.n_a + (row - plan.rows_a) * plan.cpr_b;
+  for (int j = lane; j < cnt; j += 32) chunk_merge(acc, load_partial_cg(&ws.partial[base + j]), k);
+  const float M = warp_max(acc.m);
+  const Part p = warp_combine(M, acc.m, acc.s, (acc.m - M) * k, acc.idx, acc.flags);
+  if (lane == 0) {
+    RowStat st;
+    const bool samp = k > 0.0f && M > -kInfF;
+    st.Z = samp ? p.s : 0.0f;
+    st.inv_z = samp ? __fdiv_rn(1.0f, p.s) : 0.0f;
+    st.M = M;
+    st.argmax = resolve_index<DT>(lg, row, nfull, p.idx, M);
+    st.flags = p.flags;
+    st.k = k;
+    ws.rowstat[row] = st;
   }
 }
 
 // Copy the row statistics out as plain arrays (and p at a probe token).
 __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float* out_max, int32_t* out_argmax,
                                double* out_z, float* out_p, uint32_t* row_flags) {
+  grid_dependency_wait();
   const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (row >= lg.rows) return;
   const RowStat st = ws.rowstat[row];
@@ -513,30 +806,50 @@ cudaError_t stats_occupancy(int dtype, int* blocks_per_sm) {
                                                        kStatsSmemBytes);
 }
 
-int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
+// Stages per row: 1024-vector pieces, at least one (the ragged tail rides on the last).
+int32_t stages_per_row(const LogitsView& lg) {
   const int E = lg.dtype == SV_BF16 ? 8 : 4;
-  const int64_t NVr = (lg.vocab + E - 1) / E;
-  const int64_t NV = NVr * lg.rows;
-  // One resident wave; at least ~2 vectors per thread per CTA; never more CTAs than vectors.
+  const int64_t nfull = lg.vocab / E;
+  const int64_t c = (nfull + kChunkVecs - 1) / kChunkVecs;
+  return static_cast<int32_t>(c < 1 ? 1 : c);
+}
+
+ChunkPlan chunk_plan(const LogitsView& lg, int grid) {
+  ChunkPlan P{};
+  P.nst = stages_per_row(lg);
+  P.cpr_a = (P.nst + kHeadChunkStages - 1) / kHeadChunkStages;
+  P.cpr_b = P.nst;
+  const int64_t tail_stages = static_cast<int64_t>(grid) * kTailRounds;
+  int64_t rows_b = (tail_stages + P.nst - 1) / P.nst;
+  if (rows_b > lg.rows) rows_b = lg.rows;
+  P.rows_a = static_cast<int32_t>(lg.rows - rows_b);
+  P.n_a = static_cast<int64_t>(P.rows_a) * P.cpr_a;
+  P.n_items = P.n_a + rows_b * P.cpr_b;
+  return P;
+}
+
+// One resident wave, never more CTAs than one-stage chunks (the plan then has at least as many items).
+int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
+  const int64_t cap = static_cast<int64_t>(stages_per_row(lg)) * lg.rows;
   int64_t g = static_cast<int64_t>(dev.sms) * dev.stats_blocks_per_sm[lg.dtype == SV_BF16 ? 1 : 0];
-  const int64_t by_work = (NV + 2 * kConsumers - 1) / (2 * kConsumers);
-  if (g > by_work) g = by_work;
-  if (g > kMaxStatsGrid) g = kMaxStatsGrid;
-  if (g > NV) g = NV;
+  if (g > cap) g = cap;
   if (g < 1) g = 1;
   return static_cast<int>(g);
 }
 
 cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream) {
-  const int E = lg.dtype == SV_BF16 ? 8 : 4;
-  const int64_t NVr = (lg.vocab + E - 1) / E;
-  const int64_t NV = NVr * lg.rows;
+  const ChunkPlan plan = chunk_plan(lg, grid);
+  if (plan.n_items > (int64_t{1} << 30)) return cudaErrorInvalidValue;  // chunk indices and the queue are 32-bit
+  const dim3 mgrid(static_cast<unsigned>((lg.rows + 7) / 8));
+  cudaError_t e;
   if (lg.dtype == SV_BF16) {
-    k_row_stats<SV_BF16><<<grid, kStatsThreads, kStatsSmemBytes, stream>>>(lg, map, ws, NVr, NV);
-  } else {
-    k_row_stats<SV_F32><<<grid, kStatsThreads, kStatsSmemBytes, stream>>>(lg, map, ws, NVr, NV);
+    e = launch_pdl(k_row_stats<SV_BF16>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k_row_merge<SV_BF16>, mgrid, dim3(256), 0, stream, lg, map, ws, plan);
   }
-  return cudaGetLastError();
+  e = launch_pdl(k_row_stats<SV_F32>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_row_merge<SV_F32>, mgrid, dim3(256), 0, stream, lg, map, ws, plan);
 }
 
 cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,
@@ -544,9 +857,8 @@ cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_
                                 cudaStream_t stream) {
   const int threads = 256;
   const int64_t blocks = (lg.rows + threads - 1) / threads;
-  k_export_stats<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(lg, ws, probe, out_max, out_argmax, out_z,
-                                                                        out_p, row_flags);
-  return cudaGetLastError();
+  return launch_pdl(k_export_stats, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, lg, ws, probe,
+                    out_max, out_argmax, out_z, out_p, row_flags);
 }
 
 }  // namespace sv
