@@ -18,11 +18,11 @@
 // fold each stage with packed fp32x2 arithmetic against an exponent reference
 // that moves only when a logit grows 16 log2 units past it, and at the end of
 // a chunk each warp combines its lanes and hands the result to a finalizer
-// warp, which writes the chunk's partial (maximum, the first vector holding
-// it, the sum rescaled to the maximum, flags).  k_row_merge then merges each
-// row's chunk partials in chunk order, so the result does not depend on which
-// CTA streamed what, and finds the argmax element in the one vector the merge
-// points to.  No CTA waits on another.  Every mbarrier wait is bounded (one
+// warp, which finds the chunk's argmax element in the one vector the warp
+// results point to and writes the chunk's partial (maximum, its lowest index,
+// the sum rescaled to the maximum, flags).  k_row_merge then merges each row's
+// chunk partials in chunk order, so the result does not depend on which CTA
+// streamed what.  No CTA waits on another.  Every mbarrier wait is bounded (one
 // second); a timeout raises the workspace error word, reported by the next
 // kernels as SV_DEV_TIMEOUT.
 #include <cstdint>
@@ -631,6 +631,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         break;
       }
       const int32_t item = sm.slot[sl].item;
+      const int32_t row = sm.slot[sl].row;
       const float k = sm.slot[sl].k;
       Part wp = lane < kConsumerWarps ? sm.slot[sl].wpart[lane] : part_identity();
       __syncwarp();
@@ -638,7 +639,12 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       if (item < 0) break;
       const float M = warp_max(wp.m);
       wp = warp_combine(M, wp.m, wp.s, (wp.m - M) * k, wp.idx, wp.flags);
-      if (lane == 0) ws.partial[item] = RowPartial{wp.s, wp.m, wp.idx, wp.flags};
+      if (lane == 0) {
+        // The chunk's argmax element, from the vector it lies in (just streamed, usually still in L2).
+        const int32_t idx = resolve_index<DT>(lg, row, nfull, wp.idx, M);
+        ws.partial[item] = RowPartial{wp.s, M, idx, wp.flags};
+        ws.rowstat[row].k = k;  // every chunk of the row writes the same value
+      }
     }
     return;
   }
@@ -731,19 +737,17 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
 
 // Row statistics from the chunk partials, one warp per row: merge the row's
 // chunks in chunk order (lane l takes chunks l, l+32, ...; the result does not
-// depend on which CTA streamed which chunk), find the argmax element in the
-// one vector the merge points to, and rewind the chunk queue for the next call.
+// depend on which CTA streamed which chunk; equal maxima keep the lowest
+// index), and rewind the chunk queue for the next call.
 template <int DT>
-__global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan) {
+__global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, Ws ws, ChunkPlan plan) {
   grid_dependency_wait();  // the partials come from k_row_stats
   allow_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) ws.done_cnt[2] = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x * int64_t{8} + (threadIdx.x >> 5);
   if (row >= lg.rows) return;  // whole warps leave together
-  const int64_t nfull = lg.vocab / VecTraits<DT>::E;
-  // Same k as the streaming pass used: the same map, the same function.
-  const float k = temperature_k(row_temperature(map, static_cast<int32_t>(row), lane));
+  const float k = __ldcg(&ws.rowstat[row].k);  // written by the streaming pass
   Part acc = part_identity();
   const bool head = row < plan.rows_a;
   const int32_t cnt = head ? plan.cpr_a : plan.cpr_b;
@@ -757,7 +761,7 @@ __global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, RowMap map, Ws
     st.Z = samp ? p.s : 0.0f;
     st.inv_z = samp ? __fdiv_rn(1.0f, p.s) : 0.0f;
     st.M = M;
-    st.argmax = resolve_index<DT>(lg, row, nfull, p.idx, M);
+    st.argmax = p.idx;
     st.flags = p.flags;
     st.k = k;
     ws.rowstat[row] = st;
@@ -845,11 +849,11 @@ cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& 
   if (lg.dtype == SV_BF16) {
     e = launch_pdl(k_row_stats<SV_BF16>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k_row_merge<SV_BF16>, mgrid, dim3(256), 0, stream, lg, map, ws, plan);
+    return launch_pdl(k_row_merge<SV_BF16>, mgrid, dim3(256), 0, stream, lg, ws, plan);
   }
   e = launch_pdl(k_row_stats<SV_F32>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_row_merge<SV_F32>, mgrid, dim3(256), 0, stream, lg, map, ws, plan);
+  return launch_pdl(k_row_merge<SV_F32>, mgrid, dim3(256), 0, stream, lg, ws, plan);
 }
 
 cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,
