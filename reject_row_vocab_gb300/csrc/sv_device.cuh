@@ -307,10 +307,12 @@ __device__ __forceinline__ uint64_t scale_fixed(float u, uint64_t S) {
   return (hi << (64 - sh)) | (lo >> sh);
 }
 
+// Exact warp sum of values below 2^59: the low 27 bits and the rest are summed
+// as 32-bit words by the warp-reduce unit (neither part can overflow 32 lanes).
 __device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
+  const unsigned lo = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v & ((1ull << 27) - 1)));
+  const unsigned hi = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(v >> 27));
+  return (static_cast<uint64_t>(hi) << 27) + lo;
 }
 
 __device__ __forceinline__ uint64_t warp_inclusive_scan_u64(uint64_t v) {

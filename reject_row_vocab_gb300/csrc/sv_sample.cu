@@ -92,14 +92,24 @@ __device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, boo
 __device__ __forceinline__ void weights_from_values(const float (&x)[8], const float (&qv)[8], const RowStat& rs,
                                                     float inv_z, int32_t mode, const int32_t* excl, int32_t n_excl,
                                                     int64_t col0, float (&w)[8]) {
+  // Packed pairs: each lane of a pair rounds exactly like the scalar
+  // operation, so w_i = fl(fl(ex2(fl(fl(x_i - M) * k)) / Z) - q_i) either way.
+  const float2 nM = make_float2(-rs.M, -rs.M), kk = make_float2(rs.k, rs.k), iz = make_float2(inv_z, inv_z);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float e = usable_logit(x[i]) ? ex2_fast(__fmul_rn(__fsub_rn(x[i], rs.M), rs.k)) : 0.0f;
-    w[i] = __fmul_rn(e, inv_z);
+  for (int i = 0; i < 8; i += 2) {
+    const float2 t = __fmul2_rn(__fadd2_rn(make_float2(x[i], x[i + 1]), nM), kk);
+    const float2 e = make_float2(usable_logit(x[i]) ? ex2_fast(t.x) : 0.0f, usable_logit(x[i + 1]) ? ex2_fast(t.y) : 0.0f);
+    const float2 p = __fmul2_rn(e, iz);
+    w[i] = p.x;
+    w[i + 1] = p.y;
   }
   if (mode == kModeResidual) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = fmaxf(__fsub_rn(w[i], qv[i]), 0.0f);
+    for (int i = 0; i < 8; i += 2) {
+      const float2 d = __fadd2_rn(make_float2(w[i], w[i + 1]), make_float2(-qv[i], -qv[i + 1]));
+      w[i] = fmaxf(d.x, 0.0f);
+      w[i + 1] = fmaxf(d.y, 0.0f);
+    }
   } else if (mode == kModePExcl) {
     for (int e = 0; e < n_excl; ++e) {
       const int64_t d = static_cast<int64_t>(excl[e]) - col0;
@@ -341,8 +351,21 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   const int per = (T + kSampleThreads - 1) / kSampleThreads;
   const int ta = min(T, tid * per), tb = min(T, ta + per);
 
+  // Each thread's tile sums, loaded once (all loads issued before any use)
+  // and kept in registers for both the scan and the search below.
+  constexpr int kHeld = 8;
+  const bool held = per <= kHeld;
+  uint64_t tv[kHeld];
   uint64_t loc = 0;
-  for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+  if (held) {
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j)
+      tv[j] = ta + j < tb ? __ldcg(reinterpret_cast<const unsigned long long*>(ts) + ta + j) : 0ull;
+#pragma unroll
+    for (int j = 0; j < kHeld; ++j) loc += tv[j];
+  } else {
+    for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+  }
   uint64_t total;
   uint64_t pre = block_exclusive_scan<uint64_t, kSampleThreads, NAMED>(loc, s_scan, &total);
   if (total == 0) {  // residual (or what is left of p) is empty: draw from p instead
@@ -353,7 +376,15 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
     __threadfence_block();
     group_sync<kSampleThreads, NAMED>();
     loc = 0;
-    for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    if (held) {
+#pragma unroll
+      for (int j = 0; j < kHeld; ++j)
+        tv[j] = ta + j < tb ? __ldcg(reinterpret_cast<const unsigned long long*>(ts) + ta + j) : 0ull;
+#pragma unroll
+      for (int j = 0; j < kHeld; ++j) loc += tv[j];
+    } else {
+      for (int j = ta; j < tb; ++j) loc += __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    }
     pre = block_exclusive_scan<uint64_t, kSampleThreads, NAMED>(loc, s_scan, &total);
   }
   const uint64_t t = scale_fixed(u, total);
@@ -365,7 +396,14 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   int my_tile = INT_MAX, my_nz = -1;
   uint64_t my_pre = 0, run = pre;
   for (int j = ta; j < tb; ++j) {
-    const uint64_t wj = __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    uint64_t wj = 0;
+    if (held) {
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i)
+        if (i == j - ta) wj = tv[i];
+    } else {
+      wj = __ldcg(reinterpret_cast<const unsigned long long*>(ts) + j);
+    }
     if (wj > 0) {
       my_nz = j;
       if (my_tile == INT_MAX && run <= t && t < run + wj) {
