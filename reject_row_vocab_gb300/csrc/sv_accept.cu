@@ -35,11 +35,16 @@ __device__ __forceinline__ float target_prob(float l, const RowStat& rs) {
 }
 
 __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
-  grid_dependency_wait();  // row statistics from the previous kernel
-  allow_dependents();
+  // The inputs (ids, logits, q, uniforms) were complete before the statistics
+  // pass started, and this grid starts only after that pass: the gathers below
+  // are issued before waiting for the row statistics, overlapping that wait.
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * kChainWarps + (threadIdx.x >> 5);
-  if (b >= p.batch) return;
+  if (b >= p.batch) {
+    grid_dependency_wait();
+    allow_dependents();
+    return;
+  }
   const int ML = p.max_len;
   int32_t* otok = out.out_tokens + static_cast<int64_t>(b) * ML;
   int32_t* orow = out.accept_rows + static_cast<int64_t>(b) * ML;
@@ -53,7 +58,24 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     end = p.cu[b + 1];
   }
   const int64_t L = end - start;
-  if (start < 0 || end > p.lg.rows || L < 1 || L > ML) {  // invalid layout: commit nothing
+  const bool bad_layout = start < 0 || end > p.lg.rows || L < 1 || L > ML;
+  const float T = p.temperature ? p.temperature[b] : 0.0f;
+  const bool greedy = !sampling_temperature(T);
+  // Gathers of the first 32 rows' tests (id, and for sampling l[d], q[d], u).
+  int32_t pre_d = -1;
+  float pre_l = 0.0f, pre_q = 0.0f, pre_u = 0.0f;
+  if (!bad_layout && lane < L - 1) {
+    const int64_t row = start + lane;
+    pre_d = p.ids[row + 1];
+    if (!greedy && pre_d >= 0 && pre_d < p.lg.vocab) {
+      pre_l = load_logit(p.lg, row, pre_d);
+      pre_q = p.q[row * p.ldq + pre_d];
+      pre_u = p.u_accept[row];
+    }
+  }
+  grid_dependency_wait();  // row statistics from the previous kernel
+  allow_dependents();
+  if (bad_layout) {  // invalid layout: commit nothing
     for (int k = lane; k < ML; k += 32) {
       otok[k] = -1;
       orow[k] = -1;
@@ -68,8 +90,6 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     return;
   }
 
-  const float T = p.temperature ? p.temperature[b] : 0.0f;
-  const bool greedy = !sampling_temperature(T);
   uint32_t st = __ldcg(ws.err) ? kStTimeout : 0u;
   int64_t s = L - 1;  // row (within the request) that yields the final token
   int how = 0;        // 0 all accepted, 1 rejected, 2 unusable row
@@ -84,7 +104,7 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     RowStat rs{};
     int32_t d = -1;
     if (has_row) rs = ws.rowstat[row];
-    if (tested) d = p.ids[row + 1];
+    if (tested) d = j0 == 0 ? pre_d : p.ids[row + 1];
     int stop = 0;
     uint32_t fl = rs.flags;
     if (tested) {
@@ -97,9 +117,9 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
       } else if (greedy) {
         stop = (rs.argmax != d) ? 1 : 0;
       } else {
-        const float l = load_logit(p.lg, row, d);
-        const float qd = p.q[row * p.ldq + d];
-        const float u = p.u_accept[row];
+        const float l = j0 == 0 ? pre_l : load_logit(p.lg, row, d);
+        const float qd = j0 == 0 ? pre_q : p.q[row * p.ldq + d];
+        const float u = j0 == 0 ? pre_u : p.u_accept[row];
         stop = (__fmul_rn(u, qd) < target_prob(l, rs)) ? 0 : 1;
       }
     }
@@ -162,8 +182,9 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ int32_t s_kid[kMaxNodes];
   __shared__ float s_pk[kMaxNodes];
-  grid_dependency_wait();  // row statistics from the previous kernel
-  allow_dependents();
+  // Node data and the tree's validation come from inputs that were complete
+  // before the statistics pass started (this grid starts after that pass), so
+  // they are staged before waiting for the row statistics.
   const int lane = threadIdx.x;
   const int b = blockIdx.x;
   const int N = p.nodes;
@@ -204,6 +225,8 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
 
   const float T = p.temperature ? p.temperature[b] : 0.0f;
   const bool greedy = !sampling_temperature(T);
+  grid_dependency_wait();  // row statistics from the previous kernel
+  allow_dependents();
   uint32_t st = (bad ? kStBadTree : 0u) | (__ldcg(ws.err) ? kStTimeout : 0u);
   int cur = 0, depth = 0;
   int32_t bonus = -1;
