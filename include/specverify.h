@@ -235,6 +235,44 @@ sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t 
                                   int32_t* out_argmax, double* out_z, float* out_p, uint32_t* row_flags,
                                   void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * DSpark verify-length scheduling ([E2D] §5.6.3 host budget, §5.6.4 device
+ * allocation): how many draft rows each request verifies in the next round.
+ *
+ * spec_verify_dspark_budget runs on the HOST (no GPU, host pointers).  It picks
+ * the extra draft budget K from historical survival scores: hist_survival[n]
+ * holds one score per (request, draft position) in any order; NaN scores and
+ * scores below eps are dropped, the rest sorted descending a_1 >= a_2 >= ...;
+ * with N(K) = R + a_1 + ... + a_K (predicted committed tokens) and sps[M] the
+ * speed (rounds per second) of a round with M target rows, M = 0 .. sps_len-1,
+ *   *k_star = argmax over K with R + K < sps_len of N(K) * sps[R + K]
+ * (the smaller K on ties; 0 when R >= sps_len).  Returns SV_ERR_NULL_ARG or
+ * SV_ERR_BAD_SHAPE (n < 0, num_requests < 0, sps_len < 0) on bad arguments.
+ *
+ * spec_verify_dspark_verify_lens runs on the DEVICE.  survival [R, D] (device
+ * fp32, row stride ld >= D floats) holds each request's current survival at
+ * draft positions 1..D (a running product of confidences, so non-increasing
+ * along a row).  Every (request r, position j) is a candidate; candidates are
+ * ordered by survival descending, then position ascending, then request
+ * ascending (no token id enters the order), and the first `budget` whose
+ * survival is at least eps are selected (NaN orders last and is never
+ * selected).  verify_lens[r] = clamp(1 + selected_r, min_len, max_len): one
+ * anchor row plus the selected drafts (device int32 [R]).  ws: at least
+ * spec_verify_dspark_workspace_bytes(R) bytes, zero-filled before its first
+ * use; each completed call leaves it zeroed.  Host argument errors
+ * (SV_ERR_NULL_ARG, SV_ERR_BAD_SHAPE for R, D or budget < 0, ld < D,
+ * min_len < 1, max_len < min_len, R * D > 2^30; SV_ERR_WORKSPACE_TOO_SMALL)
+ * return before anything is enqueued.
+ */
+size_t spec_verify_dspark_workspace_bytes(int32_t num_requests);
+
+sv_status_t spec_verify_dspark_budget(const float* hist_survival, int64_t n, int32_t num_requests, const float* sps,
+                                      int32_t sps_len, float eps, int32_t* k_star);
+
+sv_status_t spec_verify_dspark_verify_lens(const float* survival, int32_t num_requests, int32_t num_drafts,
+                                           int64_t ld, int32_t budget, int32_t min_len, int32_t max_len, float eps,
+                                           int32_t* verify_lens, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -142,6 +142,12 @@ thread_local cudaError_t t_last_cuda_error = cudaSuccess;
   } while (0)
 
 }  // namespace
+
+sv_status_t cuda_failure(cudaError_t e) {
+  t_last_cuda_error = e;
+  return SV_ERR_CUDA;
+}
+
 }  // namespace sv
 
 using namespace sv;

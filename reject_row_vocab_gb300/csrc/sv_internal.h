@@ -219,6 +219,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Records e as the last CUDA error of this thread and returns SV_ERR_CUDA.
+sv_status_t cuda_failure(cudaError_t e);
+
 // Device properties cached per device.
 struct DeviceInfo {
   int sms;

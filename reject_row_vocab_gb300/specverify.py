@@ -13,6 +13,7 @@ import os
 from dataclasses import dataclass
 from typing import Optional
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,8 @@ DEV_TOKEN_RANGE, DEV_NONFINITE, DEV_BAD_TREE, DEV_BAD_LAYOUT, DEV_RESIDUAL_EMPTY
 ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spec_verify_greedy_chain",
                 "spec_verify_greedy_tree", "spec_verify_rejection_chain", "spec_verify_rejection_ragged",
                 "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events",
-                "spec_verify_last_cuda_error")
+                "spec_verify_last_cuda_error", "spec_verify_rejection_chain_noalloc",
+                "spec_verify_dspark_workspace_bytes", "spec_verify_dspark_budget", "spec_verify_dspark_verify_lens")
 
 
 class SpecVerifyError(RuntimeError):
@@ -69,6 +71,9 @@ def load_library():
                                           OUT, P, SZ, P], ctypes.c_int),
         "spec_verify_row_stats": ([P, ctypes.c_int, I64, I64, I32, P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
         "spec_verify_set_stats_events": ([P, P], ctypes.c_int),
+        "spec_verify_dspark_workspace_bytes": ([I32], SZ),
+        "spec_verify_dspark_budget": ([P, I64, I32, P, I32, F, P], ctypes.c_int),
+        "spec_verify_dspark_verify_lens": ([P, I32, I32, I64, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -259,3 +264,38 @@ def row_stats(logits, row_temp=None, probe=None, ws=None, stream=None) -> dict:
         _ptr(res["argmax"]), _ptr(res["z"]), _ptr(res["p"]), _ptr(res["flags"]), _ptr(ws), ws.numel(),
         _stream(stream)))
     return res
+
+
+def dspark_budget(hist_survival, num_requests: int, sps, eps: float = 0.0) -> int:
+    """Host budget K* from historical survival scores and a speed table indexed by target rows."""
+    lib = load_library()
+    h = np.ascontiguousarray(np.asarray(hist_survival, dtype=np.float32).ravel())
+    t = np.ascontiguousarray(np.asarray(sps, dtype=np.float32).ravel())
+    k = ctypes.c_int32(-1)
+    _check("spec_verify_dspark_budget", lib.spec_verify_dspark_budget(
+        ctypes.c_void_p(h.ctypes.data) if h.size else None, h.size, int(num_requests),
+        ctypes.c_void_p(t.ctypes.data) if t.size else None, t.size, float(eps), ctypes.byref(k)))
+    return int(k.value)
+
+
+def dspark_workspace(num_requests: int, device=None) -> torch.Tensor:
+    lib = load_library()
+    return torch.zeros(int(lib.spec_verify_dspark_workspace_bytes(int(num_requests))), dtype=torch.uint8,
+                       device=device)
+
+
+def dspark_verify_lens(survival, budget: int, *, min_len: int = 1, max_len: Optional[int] = None, eps: float = 0.0,
+                       out=None, ws=None, stream=None) -> torch.Tensor:
+    """verify_lens [R] (int32, on survival's device) from the current survival [R, D]."""
+    lib = load_library()
+    R, D = survival.shape
+    if max_len is None:
+        max_len = D + 1
+    if out is None:
+        out = torch.empty(R, dtype=torch.int32, device=survival.device)
+    if ws is None:
+        ws = dspark_workspace(R, survival.device)
+    _check("spec_verify_dspark_verify_lens", lib.spec_verify_dspark_verify_lens(
+        _ptr(survival), R, D, survival.stride(0), int(budget), int(min_len), int(max_len), float(eps), _ptr(out),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
