@@ -106,6 +106,41 @@ def verify_chain(w, greedy_all: bool = False, threads: int = 1, cu_seqlens=None,
     return o
 
 
+def scatter_candidates(cand_ids, cand_probs, vocab: int):
+    """Dense q from candidate lists, [E2D] §6.5: the selector's sparse q is
+    scattered into vocabulary coordinates (zero elsewhere) before rejection.
+
+    Returns (q [R, vocab] float32, bad [R] bool).  Id -1 is padding; any other
+    id outside [0, vocab) is left out of q and marks its row bad.  Repeated ids
+    add up (accumulated in fp64).
+    """
+    ids = np.asarray(cand_ids, dtype=np.int64)
+    pr = np.asarray(cand_probs, dtype=np.float64)
+    R, K = ids.shape
+    ok = (ids >= 0) & (ids < vocab)
+    bad = np.any((ids != -1) & ~ok, axis=1)
+    q = np.zeros((R, vocab), dtype=np.float64)
+    rr = np.repeat(np.arange(R), K).reshape(R, K)
+    np.add.at(q, (rr[ok], ids[ok]), pr[ok])
+    return q.astype(np.float32), bad
+
+
+def verify_chain_sparse(w, threads: int = 1) -> dict:
+    """Oracle outputs for a chain whose q is given as candidate lists: the
+    dense chain verification over the scattered q.  A request is flagged
+    SV_DEV_TOKEN_RANGE (bit 1) when a tested row (every row but its last) has a
+    candidate id outside [0, vocab) other than the padding -1."""
+    import dataclasses
+    q, bad = scatter_candidates(w.cand_ids, w.cand_probs, w.vocab)
+    dense = dataclasses.replace(w, q=q, kind="rejection_chain")
+    o = verify_chain(dense, threads=threads)
+    cu = np.asarray(w.cu_seqlens, dtype=np.int64)
+    for b in range(len(cu) - 1):
+        if cu[b + 1] - 1 > cu[b] and bad[cu[b]:cu[b + 1] - 1].any():
+            o["status"][b] |= np.uint32(1)
+    return o
+
+
 def verify_tree(w, mode: str, threads: int = 1, use_lists: bool = False) -> dict:
     """Oracle outputs for a tree workload; mode 'greedy' or 'target_only'."""
     lib = _load()

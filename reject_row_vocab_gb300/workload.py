@@ -50,7 +50,8 @@ def uniforms(rng: np.random.Generator, n: int) -> np.ndarray:
 # Workload container
 # ----------------------------------------------------------------------------
 
-KINDS = ("greedy_chain", "rejection_chain", "rejection_ragged", "greedy_tree", "target_only_tree")
+KINDS = ("greedy_chain", "rejection_chain", "rejection_ragged", "greedy_tree", "target_only_tree",
+         "rejection_chain_sparse")
 
 
 @dataclass
@@ -68,6 +69,8 @@ class Workload:
     cu_seqlens: Optional[np.ndarray] = None   # int32 [B+1]
     verify_ids: Optional[np.ndarray] = None   # int32 [rows] (row i input token; row i tests verify_ids[i+1])
     q: Optional[np.ndarray] = None            # float32 [rows, vocab]
+    cand_ids: Optional[np.ndarray] = None     # int32 [rows, K]: sparse q ids (-1 pads)
+    cand_probs: Optional[np.ndarray] = None   # float32 [rows, K]: sparse q probabilities
     temperature: Optional[np.ndarray] = None  # float32 [B]
     u_accept: Optional[np.ndarray] = None     # float32 [rows]
     u_final: Optional[np.ndarray] = None      # float32 [B]
@@ -90,7 +93,8 @@ class Workload:
 
     def arrays(self) -> dict:
         out = {}
-        for k in ("logits", "cu_seqlens", "verify_ids", "q", "temperature", "u_accept", "u_final",
+        for k in ("logits", "cu_seqlens", "verify_ids", "q", "cand_ids", "cand_probs", "temperature", "u_accept",
+                  "u_final",
                   "tokens", "parents", "first_child", "next_sibling", "row_slots", "seq_lens"):
             v = getattr(self, k)
             if v is not None:
@@ -216,6 +220,58 @@ def rejection_chain(batch: int = 8, m: int = 7, vocab: int = 151936, dtype: str 
                     seq_lens=rng.integers(128, 4097, size=batch).astype(np.int64),
                     meta={"seed": seed, "sigma": sigma, "boost": boost, "T": temperature,
                           "noise_sigma": noise_sigma})
+
+
+def rejection_chain_sparse(batch: int = 8, m: int = 7, vocab: int = 151936, dtype: str = "bf16", K: int = 16,
+                           sigma: float = 3.0, boost: float = 6.0, temperature: float = 0.8, noise_sigma: float = 1.0,
+                           pad: int = 0, seed: int = 1006, name: str = "rejection_chain_sparse") -> Workload:
+    """p/q rejection chain whose q has K nonzeros (a candidate selector, [E2D] §6.2, §6.5).
+
+    Per row the drafter scores every id with l/T + noise, keeps the K best as
+    candidates (score order), sets q = softmax over the candidates' scores and
+    draws the draft by inverse CDF over the candidates in that order.  `pad`
+    trailing entries per row carry id -1 (padding) with a nonzero probability
+    that must be ignored.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    L = m + 1
+    R = batch * L
+    x = _gaussian_logits(rng, R, vocab, sigma)
+    if boost:
+        hot = rng.integers(0, vocab, size=R)
+        x[np.arange(R), hot] += np.float32(boost)
+    logits = _to_storage(x, dtype)
+    xv = _as_f32(logits, dtype)
+    T = np.full(batch, temperature, dtype=np.float32)
+    Kc = min(K, vocab)
+    cand = np.full((R, Kc + pad), -1, dtype=np.int32)
+    prob = np.zeros((R, Kc + pad), dtype=np.float32)
+    d = np.empty(R, dtype=np.int32)
+    u = rng.random(R)
+    for r in range(R):
+        z = xv[r].astype(np.float64) / float(np.float32(temperature))
+        z += noise_sigma * rng.standard_normal(vocab)
+        top = np.argpartition(-z, Kc - 1)[:Kc]
+        top = top[np.argsort(-z[top], kind="stable")]
+        e = np.exp(z[top] - z[top].max())
+        pr = e / e.sum()
+        cand[r, :Kc] = top
+        prob[r, :Kc] = pr
+        prob[r, Kc:] = 0.5
+        c = np.cumsum(pr)
+        d[r] = top[min(int(np.searchsorted(c, u[r] * c[-1], side="right")), Kc - 1)]
+    ids = rng.integers(0, vocab, size=R, dtype=np.int64).astype(np.int32)
+    for b in range(batch):
+        for j in range(m):
+            ids[b * L + j + 1] = d[b * L + j]
+    cu = (np.arange(batch + 1, dtype=np.int64) * L).astype(np.int32)
+    return Workload(kind="rejection_chain_sparse", name=name, dtype=dtype, logits=logits, batch=batch,
+                    vocab=vocab, rows=R, max_len=L, m=m, cu_seqlens=cu, verify_ids=ids, cand_ids=cand,
+                    cand_probs=prob, temperature=T, u_accept=uniforms(rng, R), u_final=uniforms(rng, batch),
+                    row_slots=rng.permutation(1 << 20)[:R].astype(np.int64),
+                    seq_lens=rng.integers(128, 4097, size=batch).astype(np.int64),
+                    meta={"seed": seed, "sigma": sigma, "boost": boost, "T": temperature, "K": K,
+                          "noise_sigma": noise_sigma, "pad": pad})
 
 
 def ragged_block(batch: int = 256, max_len: int = 8, vocab: int = 151936, dtype: str = "bf16",
