@@ -30,8 +30,9 @@ if ROOT not in sys.path:
 
 METRIC = "verified rows/s"
 UNIT = "rows/s"
-KERNELS_PER_STEP = {"greedy_chain": 3, "greedy_tree": 3, "rejection_chain": 3, "rejection_ragged": 3,
-                    "target_only_tree": 3}
+# statistics, row merge, acceptance, then the sampler (with the commit) or the commit alone
+KERNELS_PER_STEP = {"greedy_chain": 4, "greedy_tree": 4, "rejection_chain": 4, "rejection_ragged": 4,
+                    "target_only_tree": 4, "rejection_chain_sparse": 4}
 STATS_SOURCES = ("reject_row_vocab_gb300/csrc/sv_stats.cu", "reject_row_vocab_gb300/csrc/sv_device.cuh")
 
 
@@ -46,6 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--eager", action="store_true", help="launch every step from Python instead of a CUDA graph")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--q-cands", type=int, default=0,
+                    help="rejection chains only: q given as K candidates per row (sparse) instead of dense rows")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
@@ -212,6 +215,15 @@ def stats_traffic() -> float | None:
 
 def make_workload(args, rank: int = 0):
     from reject_row_vocab_gb300 import workload as wl
+    if args.q_cands > 0:  # the same chain shape with a K-candidate (selector) q instead of dense q rows
+        if args.config not in (2, 4):
+            raise SystemExit("--q-cands applies to the rejection-chain workloads (2, 4)")
+        shape = {2: dict(batch=8, m=7, boost=6.0, temperature=0.8, noise_sigma=1.0, name="c2_rejection_chain"),
+                 4: dict(batch=64, m=15, boost=0.0, temperature=1.0, noise_sigma=1.5, name="c4_dflash_block")}
+        kw = dict(shape[args.config])
+        kw["name"] += "_sparse_q%d" % args.q_cands
+        return wl.rejection_chain_sparse(vocab=151936, dtype="bf16", K=args.q_cands, sigma=3.0,
+                                         seed=rank_seed(args.config, rank), **kw)
     kw = {"seed": rank_seed(args.config, rank)}
     if args.config == 3:
         kw["mode"] = args.tree_mode
@@ -232,6 +244,8 @@ def oracle_run(w, threads: int):
         return oracle.verify_chain(w, greedy_all=True, threads=threads)
     if w.kind in ("rejection_chain", "rejection_ragged"):
         return oracle.verify_chain(w, threads=threads)
+    if w.kind == "rejection_chain_sparse":
+        return oracle.verify_chain_sparse(w, threads=threads)
     return oracle.verify_tree(w, "greedy" if w.kind == "greedy_tree" else "target_only", threads=threads)
 
 

@@ -161,6 +161,31 @@ sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, in
                                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * p/q rejection chain with a SPARSE q ([E2D] §6.2, §6.5: a candidate selector
+ * proposes from K candidates; its q is zero outside them, and tokens outside
+ * the candidates can still come out through the residual [p - q]_+).  Same
+ * arguments and results as spec_verify_rejection_chain, with q replaced by
+ * candidate lists: cand_ids / cand_probs [rows, ldc] (device int32 / fp32,
+ * ldc >= num_cands, 1 <= num_cands <= 1024); row i's list describes the q that
+ * proposed verify_ids[i + 1]: q_i(v) = the sum of cand_probs[i][c] over c with
+ * cand_ids[i][c] == v.  Id -1 is padding; any other id outside [0, vocab) is
+ * ignored and sets SV_DEV_TOKEN_RANGE for the request when it appears in one of
+ * the request's tested rows (all rows but its last).  No dense q is read or
+ * formed.  ws: at least spec_verify_sparse_workspace_bytes(batch * (m + 1),
+ * batch, vocab, m + 1, num_cands) bytes (same rules as every workspace).
+ */
+size_t spec_verify_sparse_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len,
+                                          int32_t num_cands);
+
+sv_status_t spec_verify_rejection_chain_sparse(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                               int32_t m, int32_t vocab, const int32_t* verify_ids,
+                                               const int32_t* cand_ids, const float* cand_probs, int32_t num_cands,
+                                               int64_t ldc, const float* temperature, const float* u_accept,
+                                               const float* u_final, const int64_t* row_slots,
+                                               const int64_t* seq_lens, const sv_out_t* out, void* ws,
+                                               size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Ragged p/q rejection ([E2D] §5.6.5: verify_lens include the anchor, compact
  * offsets, e.g. lens [4,2,6] -> [0,4,6,12]).  Request b owns rows
  * [cu_seqlens[b], cu_seqlens[b+1]) of the total_rows rows; lengths must lie in

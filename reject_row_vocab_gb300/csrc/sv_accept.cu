@@ -34,6 +34,75 @@ __device__ __forceinline__ float target_prob(float l, const RowStat& rs) {
   return __fdiv_rn(exp2f((l - rs.M) * rs.k), rs.Z);
 }
 
+// q(d) of a sparse row: the sum of the candidate probabilities whose id is d
+// (in candidate order); *bad is set when an id other than the padding -1
+// falls outside [0, V).
+__device__ __forceinline__ float sparse_q_at(const ChainParams& p, int64_t row, int32_t d, bool* bad) {
+  const int32_t* ids = p.cand_ids + row * p.ldc;
+  const float* pr = p.cand_probs + row * p.ldc;
+  constexpr int U = 8;  // loads issued together, one round trip per U candidates
+  float q = 0.0f;
+  for (int c0 = 0; c0 < p.num_cands; c0 += U) {
+    int32_t id[U];
+    float pv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      id[u] = c0 + u < p.num_cands ? ids[c0 + u] : -1;
+      pv[u] = c0 + u < p.num_cands ? pr[c0 + u] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (id[u] == d) q = __fadd_rn(q, pv[u]);
+      if (id[u] != -1 && (id[u] < 0 || id[u] >= p.lg.vocab)) *bad = true;
+    }
+  }
+  return q;
+}
+
+// The candidates of a sparse residual row, valid ids only, sorted by id (equal
+// ids keep their candidate order), into the request's workspace list; returns
+// their number.  The whole warp takes part.
+__device__ __forceinline__ int32_t write_sorted_candidates(const ChainParams& p, int64_t row, int32_t* cid,
+                                                           float* cq) {
+  const int lane = threadIdx.x & 31;
+  const int32_t* ids = p.cand_ids + row * p.ldc;
+  const float* pr = p.cand_probs + row * p.ldc;
+  const int K = p.num_cands, V = p.lg.vocab;
+  int32_t n_valid = 0;
+  if (K <= 32) {  // one candidate per lane: ranks from shuffles, no reloads
+    const int32_t id = lane < K ? ids[lane] : -1;
+    const float pv = lane < K ? pr[lane] : 0.0f;
+    const bool ok = lane < K && id >= 0 && id < V;
+    n_valid = __popc(__ballot_sync(kFull, ok));
+    int rank = 0;  // valid candidates ordered before this one (by id, then position)
+    for (int o = 0; o < 32; ++o) {
+      const int32_t oid = __shfl_sync(kFull, id, o);
+      const bool ook = o < K && oid >= 0 && oid < V;
+      if (ook && (oid < id || (oid == id && o < lane))) ++rank;
+    }
+    if (ok) {
+      cid[rank] = id;
+      cq[rank] = pv;
+    }
+    return n_valid;
+  }
+  for (int c0 = 0; c0 < K; c0 += 32) {
+    const int c = c0 + lane;
+    const int32_t id = c < K ? ids[c] : -1;
+    n_valid += __popc(__ballot_sync(kFull, c < K && id >= 0 && id < V));
+    if (c < K && id >= 0 && id < V) {
+      int rank = 0;  // valid candidates ordered before this one
+      for (int o = 0; o < K; ++o) {
+        const int32_t oid = ids[o];
+        if (oid >= 0 && oid < V && (oid < id || (oid == id && o < c))) ++rank;
+      }
+      cid[rank] = id;
+      cq[rank] = pr[c];
+    }
+  }
+  return n_valid;
+}
+
 __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
   // The inputs (ids, logits, q, uniforms) were complete before the statistics
   // pass started, and this grid starts only after that pass: the gathers below
@@ -62,15 +131,24 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
   const float T = p.temperature ? p.temperature[b] : 0.0f;
   const bool greedy = !sampling_temperature(T);
   // Gathers of the first 32 rows' tests (id, and for sampling l[d], q[d], u).
+  const bool sparse = p.cand_ids != nullptr;
   int32_t pre_d = -1;
   float pre_l = 0.0f, pre_q = 0.0f, pre_u = 0.0f;
-  if (!bad_layout && lane < L - 1) {
-    const int64_t row = start + lane;
-    pre_d = p.ids[row + 1];
-    if (!greedy && pre_d >= 0 && pre_d < p.lg.vocab) {
-      pre_l = load_logit(p.lg, row, pre_d);
-      pre_q = p.q[row * p.ldq + pre_d];
-      pre_u = p.u_accept[row];
+  bool cand_bad = false;  // a tested row lists a candidate id outside [0, V)
+  for (int64_t j = lane; !bad_layout && j < L - 1; j += 32) {
+    const int64_t row = start + j;
+    const int32_t d = p.ids[row + 1];
+    if (sparse) {  // every tested row's list is checked, visited or not
+      const float qd = sparse_q_at(p, row, d, &cand_bad);
+      if (j == lane) pre_q = qd;
+    }
+    if (j == lane) {
+      pre_d = d;
+      if (!greedy && d >= 0 && d < p.lg.vocab) {
+        pre_l = load_logit(p.lg, row, d);
+        if (!sparse) pre_q = p.q[row * p.ldq + d];
+        pre_u = p.u_accept[row];
+      }
     }
   }
   grid_dependency_wait();  // row statistics from the previous kernel
@@ -90,7 +168,7 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     return;
   }
 
-  uint32_t st = __ldcg(ws.err) ? kStTimeout : 0u;
+  uint32_t st = (__ldcg(ws.err) ? kStTimeout : 0u) | (warp_or(cand_bad ? 1u : 0u) ? kStTokenRange : 0u);
   int64_t s = L - 1;  // row (within the request) that yields the final token
   int how = 0;        // 0 all accepted, 1 rejected, 2 unusable row
   RowStat fs{};
@@ -117,8 +195,9 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
       } else if (greedy) {
         stop = (rs.argmax != d) ? 1 : 0;
       } else {
+        bool unused = false;
         const float l = j0 == 0 ? pre_l : load_logit(p.lg, row, d);
-        const float qd = j0 == 0 ? pre_q : p.q[row * p.ldq + d];
+        const float qd = j0 == 0 ? pre_q : (sparse ? sparse_q_at(p, row, d, &unused) : p.q[row * p.ldq + d]);
         const float u = j0 == 0 ? pre_u : p.u_accept[row];
         stop = (__fmul_rn(u, qd) < target_prob(l, rs)) ? 0 : 1;
       }
@@ -153,8 +232,12 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
   } else if (greedy) {
     bonus = fs.argmax;
   } else {
-    mode = (how == 1) ? kModeResidual : kModeP;
+    mode = (how == 1) ? (sparse ? kModeResidualSparse : kModeResidual) : kModeP;
   }
+  int32_t n_list = 0;
+  if (mode == kModeResidualSparse)
+    n_list = write_sorted_candidates(p, fr, ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap,
+                                     ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap);
   for (int64_t k = lane; k < ML; k += 32) {
     int32_t t = -1, r = -1;
     if (k < s) {
@@ -172,7 +255,7 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     out.num_out[b] = static_cast<int32_t>(s + 1);
     out.bonus[b] = bonus;
     out.dev_status[b] = st;
-    ws.state[b] = ReqState{static_cast<int32_t>(s), static_cast<int32_t>(fr), mode, bonus, st, 0, 0, 0};
+    ws.state[b] = ReqState{static_cast<int32_t>(s), static_cast<int32_t>(fr), mode, bonus, st, n_list, 0, 0};
   }
 }
 

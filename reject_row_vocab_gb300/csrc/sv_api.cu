@@ -73,8 +73,9 @@ sv_status_t check_out(const sv_out_t* out, const int64_t* row_slots, const int64
   return SV_OK;
 }
 
-sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, Ws* w) {
-  const WsLayout L = ws_layout(rows, batch, vocab, max_len);
+sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, Ws* w,
+                  int32_t num_cands = 0) {
+  const WsLayout L = ws_layout(rows, batch, vocab, max_len, num_cands);
   if (!ws || ws_bytes < L.total || !aligned(ws, 256)) return SV_ERR_WORKSPACE_TOO_SMALL;
   char* base = static_cast<char*>(ws);
   w->chunk_cnt = reinterpret_cast<uint32_t*>(base + L.chunk_cnt);
@@ -84,6 +85,9 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   w->partial = reinterpret_cast<RowPartial*>(base + L.partial);
   w->state = reinterpret_cast<ReqState*>(base + L.state);
   w->excl = reinterpret_cast<int32_t*>(base + L.excl);
+  w->cand_id = reinterpret_cast<int32_t*>(base + L.cand);
+  w->cand_q = reinterpret_cast<float*>(base + L.cand + 4 * static_cast<size_t>(batch > 0 ? batch : 1) * L.cand_cap);
+  w->cand_cap = L.cand_cap;
   w->tsum = reinterpret_cast<uint64_t*>(base + L.tsum);
   w->ntiles = L.ntiles;
   return SV_OK;
@@ -209,16 +213,22 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
                                     const int32_t* verify_ids, const float* q, int64_t ldq,
                                     const float* temperature, const float* u_accept, const float* u_final,
                                     const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
-                                    void* ws, size_t ws_bytes, cudaStream_t stream) {
+                                    void* ws, size_t ws_bytes, cudaStream_t stream, const int32_t* cand_ids = nullptr,
+                                    const float* cand_probs = nullptr, int32_t num_cands = 0, int64_t ldc = 0) {
   if (batch > 65535) return SV_ERR_BAD_SHAPE;  // the sampler's grid has one y-slice per request
   if (batch == 0) return empty_batch(out, stream);
   SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
   if (!verify_ids || !temperature || !u_accept || !u_final) return SV_ERR_NULL_ARG;
   if (fixed_len == 0 && !cu) return SV_ERR_NULL_ARG;
-  SV_TRY(check_q(q, ldq, vocab));
+  if (cand_ids) {  // sparse q: candidate lists instead of dense rows
+    if (!cand_probs) return SV_ERR_NULL_ARG;
+    if (num_cands < 1 || num_cands > kMaxCands || ldc < num_cands) return SV_ERR_BAD_SHAPE;
+  } else {
+    SV_TRY(check_q(q, ldq, vocab));
+  }
   SV_TRY(check_out(out, row_slots, seq_lens));
   Ws w{};
-  SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w));
+  SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w, cand_ids ? num_cands : 0));
   DeviceInfo dev{};
   SV_TRY_CUDA(device_info(&dev));
   const LogitsView lg{logits, dtype, ld, rows, vocab};
@@ -228,10 +238,11 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
                                      : RowMap{kMapCu, 0, batch, cu, temperature};
     SV_TRY_CUDA(row_stats_timed(lg, map, w, stats_grid(dev, lg), stream));
   }
-  ChainParams p{lg, batch, max_len, fixed_len, cu, verify_ids, q, ldq, temperature, u_accept, u_final};
+  ChainParams p{lg,       batch,    max_len,  fixed_len, cu,        verify_ids, q,  ldq,
+                temperature, u_accept, u_final, cand_ids, cand_probs, num_cands, ldc};
   SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
-  SV_TRY_CUDA(launch_sample_and_commit(lg, q, ldq, u_final, ov, CommitParams{batch, max_len, row_slots, seq_lens, w.err}, w,
-                                       dev, stream));
+  SV_TRY_CUDA(launch_sample_and_commit(lg, q, ldq, u_final, ov, CommitParams{batch, max_len, row_slots, seq_lens, w.err},
+                                       w, dev, stream, cand_ids != nullptr));
   return SV_OK;
 }
 
@@ -244,6 +255,26 @@ sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, in
   const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
   return rejection_common(logits, dtype, ld, batch, rows, m + 1, m + 1, vocab, nullptr, verify_ids, q, ldq,
                           temperature, u_accept, u_final, row_slots, seq_lens, out, ws, ws_bytes, stream);
+}
+
+size_t spec_verify_sparse_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len,
+                                          int32_t num_cands) {
+  return ws_layout(rows, batch, vocab, max_len, num_cands).total;
+}
+
+sv_status_t spec_verify_rejection_chain_sparse(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                               int32_t m, int32_t vocab, const int32_t* verify_ids,
+                                               const int32_t* cand_ids, const float* cand_probs, int32_t num_cands,
+                                               int64_t ldc, const float* temperature, const float* u_accept,
+                                               const float* u_final, const int64_t* row_slots,
+                                               const int64_t* seq_lens, const sv_out_t* out, void* ws,
+                                               size_t ws_bytes, cudaStream_t stream) {
+  if (batch < 0 || m < 0 || m >= (1 << 20)) return SV_ERR_BAD_SHAPE;
+  if (batch > 0 && !cand_ids) return SV_ERR_NULL_ARG;
+  const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
+  return rejection_common(logits, dtype, ld, batch, rows, m + 1, m + 1, vocab, nullptr, verify_ids, nullptr, 0,
+                          temperature, u_accept, u_final, row_slots, seq_lens, out, ws, ws_bytes, stream, cand_ids,
+                          cand_probs, num_cands, ldc);
 }
 
 sv_status_t spec_verify_rejection_ragged(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,

@@ -56,7 +56,8 @@ enum SampleMode : int32_t {
   kModeResidual = 1,   // draw from [p - q]_+ of sample_row
   kModeP = 2,          // draw from p of sample_row (bonus)
   kModePExcl = 3,      // draw from p of sample_row with the excluded tokens zeroed
-  kModeNoCommit = 4    // bad layout: nothing to do
+  kModeNoCommit = 4,   // bad layout: nothing to do
+  kModeResidualSparse = 5  // draw from [p - q]_+ of sample_row, q given as the request's candidate list
 };
 
 struct ReqState {
@@ -78,13 +79,14 @@ constexpr int kMaxNodes = 1024;
 
 struct WsLayout {
   size_t chunk_cnt, done_cnt, counters_end;
-  size_t rowstat, partial, state, excl, tsum, total;
+  size_t rowstat, partial, state, excl, cand, tsum, total;
+  int32_t cand_cap;  // candidate-list entries per request (sparse q), at least 1
   int32_t ntiles;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len) {
+inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, int32_t num_cands = 0) {
   WsLayout L{};
   size_t off = 0;
   L.chunk_cnt = off;
@@ -106,6 +108,9 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
   L.excl = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
                            static_cast<size_t>(max_len > 0 ? max_len : 1), 256);
+  L.cand = off;  // per request: the residual row's candidates sorted by id (id, probability)
+  L.cand_cap = num_cands > 0 ? num_cands : 1;
+  off = align_up(off + 8 * static_cast<size_t>(batch > 0 ? batch : 1) * static_cast<size_t>(L.cand_cap), 256);
   L.ntiles = (vocab + kTile - 1) / kTile;
   L.tsum = off;
   off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
@@ -123,6 +128,9 @@ struct Ws {
   RowPartial* partial;
   ReqState* state;
   int32_t* excl;
+  int32_t* cand_id;  // [B, cand_cap] sorted candidate ids of a sparse residual row
+  float* cand_q;     // [B, cand_cap] their probabilities
+  int32_t cand_cap;
   uint64_t* tsum;  // fixed-point tile sums of the sampled rows
   int32_t ntiles;
 };
@@ -175,7 +183,14 @@ struct ChainParams {
   const float* temperature;   // NULL: greedy for every request
   const float* u_accept;
   const float* u_final;
+  const int32_t* cand_ids;    // sparse q: [rows, ldc] candidate ids (-1 pads), NULL for dense q
+  const float* cand_probs;    // [rows, ldc] their probabilities
+  int32_t num_cands;
+  int64_t ldc;
 };
+
+// Largest candidate list per row a sparse q may have.
+constexpr int kMaxCands = 1024;
 
 struct TreeParams {
   LogitsView lg;
@@ -240,7 +255,7 @@ cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws
 // Residual / bonus sampler (two passes) followed by the commit, or the commit alone.
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
-                                     const DeviceInfo& dev, cudaStream_t stream);
+                                     const DeviceInfo& dev, cudaStream_t stream, bool sparse_q = false);
 cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream);
 cudaError_t sample_smem_setup();
 

@@ -30,7 +30,7 @@ constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kCommitThreads = 256;
 
 __device__ __forceinline__ bool sampling_mode(int32_t mode) {
-  return mode == kModeResidual || mode == kModeP || mode == kModePExcl;
+  return mode == kModeResidual || mode == kModeP || mode == kModePExcl || mode == kModeResidualSparse;
 }
 
 // Raw 16-byte loads of one lane's eight entries (logits, and q for a residual).
@@ -89,9 +89,16 @@ __device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, boo
 
 // Weights of eight entries from their values; the single definition both
 // passes use, so a tile's weights are bit-identical in both.
+// SP: the kernel serves sparse-q requests (kModeResidualSparse); without it
+// that mode is compiled out.  For kModePExcl (excl, n_excl) lists the tokens to zero; for
+// kModeResidualSparse (excl, excl_q, n_excl) is the row's candidate list
+// sorted by id, and w = max(p - q, 0) with q the list's probabilities,
+// subtracted in list order.
+template <bool SP>
 __device__ __forceinline__ void weights_from_values(const float (&x)[8], const float (&qv)[8], const RowStat& rs,
-                                                    float inv_z, int32_t mode, const int32_t* excl, int32_t n_excl,
-                                                    int64_t col0, float (&w)[8]) {
+                                                    float inv_z, int32_t mode, const int32_t* excl,
+                                                    const float* excl_q, int32_t n_excl, int64_t col0,
+                                                    float (&w)[8]) {
   // Packed pairs: each lane of a pair rounds exactly like the scalar
   // operation, so w_i = fl(fl(ex2(fl(fl(x_i - M) * k)) / Z) - q_i) either way.
   const float2 nM = make_float2(-rs.M, -rs.M), kk = make_float2(rs.k, rs.k), iz = make_float2(inv_z, inv_z);
@@ -103,7 +110,7 @@ __device__ __forceinline__ void weights_from_values(const float (&x)[8], const f
     w[i] = p.x;
     w[i + 1] = p.y;
   }
-  if (mode == kModeResidual) {
+  if (!SP && mode == kModeResidual) {
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {
       const float2 d = __fadd2_rn(make_float2(w[i], w[i + 1]), make_float2(-qv[i], -qv[i + 1]));
@@ -117,15 +124,56 @@ __device__ __forceinline__ void weights_from_values(const float (&x)[8], const f
       for (int i = 0; i < 8; ++i)
         if (d == i) w[i] = 0.0f;
     }
+  } else if (SP && mode == kModeResidualSparse) {
+    for (int e = 0; e < n_excl; ++e) {
+      const int64_t d = static_cast<int64_t>(excl[e]) - col0;
+      if (d >= 0 && d < 8) {
+        const float qe = excl_q[e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (d == i) w[i] = __fsub_rn(w[i], qe);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = fmaxf(w[i], 0.0f);
   }
+}
+
+// The same candidate subtraction for a whole tile [t0, t0 + 256) at once: the
+// warp finds the (rare) candidates inside the tile with a ballot and the
+// owning lane subtracts them, in list order, so the result equals the lane
+// loop of weights_from_values exactly.  w holds p on entry.
+__device__ __forceinline__ void apply_candidates_tile(float (&w)[8], int64_t t0, int lane, const int32_t* cid,
+                                                      const float* cq, int32_t n) {
+  for (int g = 0; g < n; g += 32) {
+    const int c = g + lane;
+    const int32_t id = c < n ? cid[c] : -1;
+    const float qq = c < n ? cq[c] : 0.0f;
+    const int64_t off = static_cast<int64_t>(id) - t0;
+    unsigned hit = __ballot_sync(0xffffffffu, c < n && off >= 0 && off < kTile);
+    while (hit) {
+      const int src = __ffs(hit) - 1;
+      hit &= hit - 1;
+      const int o = static_cast<int>(__shfl_sync(0xffffffffu, off, src));
+      const float hq = __shfl_sync(0xffffffffu, qq, src);
+      if ((o >> 3) == lane) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((o & 7) == i) w[i] = __fsub_rn(w[i], hq);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = fmaxf(w[i], 0.0f);
 }
 
 // The eight weights of one lane of a tile: entries [col0, col0 + 8) of `row`.
 // Entries past the vocabulary weigh 0.
+template <bool SP>
 __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
                                              const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
-                                             int32_t n_excl, int64_t col0, float (&w)[8]) {
-  const bool resid = mode == kModeResidual;
+                                             const float* excl_q, int32_t n_excl, int64_t col0, float (&w)[8]) {
+  const bool resid = !SP && mode == kModeResidual;  // a sparse-q kernel never reads dense q
   float x[8], qv[8];
   if (col0 + 8 <= lg.vocab) {
     LaneRaw r;
@@ -139,7 +187,7 @@ __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* 
       qv[i] = (resid && in) ? __ldg(q + row * ldq + col0 + i) : 0.0f;
     }
   }
-  weights_from_values(x, qv, rs, inv_z, mode, excl, n_excl, col0, w);
+  weights_from_values<SP>(x, qv, rs, inv_z, mode, excl, excl_q, n_excl, col0, w);
 }
 
 // A lane's weight sum: fp32, left to right.  Pass B walks the same additions.
@@ -276,8 +324,8 @@ __device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const flo
         }
         float x[8], qv[8], w[8];
         lane_unpack(r, DT, RESID, x, qv);
-        weights_from_values(x, qv, rs, inv_z, mode, excl, n_excl, static_cast<int64_t>(t0 + u) * kTile + lane * 8,
-                            w);
+        weights_from_values<false>(x, qv, rs, inv_z, mode, excl, nullptr, n_excl,
+                            static_cast<int64_t>(t0 + u) * kTile + lane * 8, w);
         ls[u] = lane_sum(w);
       }
     } else {
@@ -285,8 +333,8 @@ __device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const flo
       for (int u = 0; u < U; ++u) {
         float w[8];
         if (t0 + u < tb) {
-          lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, n_excl, static_cast<int64_t>(t0 + u) * kTile + lane * 8,
-                       w);
+          lane_weights<false>(lg, q, ldq, row, rs, inv_z, mode, excl, nullptr, n_excl,
+                       static_cast<int64_t>(t0 + u) * kTile + lane * 8, w);
           ls[u] = lane_sum(w);
         } else {
           ls[u] = 0.0f;
@@ -332,7 +380,7 @@ __device__ __forceinline__ void warp_tile_sums(const LogitsView& lg, const float
 // (exact, fixed-point) tile sums, pick the tile holding T = floor(u_final * S),
 // then one warp re-forms that tile's weights (same arithmetic as the sums) and
 // walks to the entry.  rs is the sampled row's statistics, u its uniform.
-template <bool NAMED>
+template <bool NAMED, bool SP>
 __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q, int64_t ldq, float u,
                                            const OutView& out, const CommitParams& cp, const Ws& ws,
                                            int32_t excl_stride, int b, const ReqState& rq, const RowStat& rs) {
@@ -344,7 +392,10 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   const int T = ws.ntiles;
   const int64_t row = rq.sample_row;
   const float inv_z = inverse_z(rs);
-  const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
+  const bool sparse = SP && rq.mode == kModeResidualSparse;
+  const int32_t* excl = sparse ? ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap
+                               : ws.excl + static_cast<int64_t>(b) * excl_stride;
+  const float* excl_q = sparse ? ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap : nullptr;
   uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
   int32_t mode = rq.mode;
   uint32_t st_add = 0u;
@@ -427,7 +478,8 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
     const uint64_t tpre = located ? s_pre : 0;
     const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
     float w[8];
-    lane_weights(lg, q, ldq, row, rs, inv_z, mode, excl, mode == kModePExcl ? rq.n_excl : 0, col0, w);
+    lane_weights<SP>(lg, q, ldq, row, rs, inv_z, mode, excl, excl_q,
+                 (mode == kModePExcl || mode == kModeResidualSparse) ? rq.n_excl : 0, col0, w);
     const uint64_t W = to_fixed(lane_sum(w));
     const uint64_t li = warp_inclusive_scan_u64(W);
     const uint64_t lo = tpre + (li - W), hi = tpre + li;
@@ -496,6 +548,7 @@ __device__ __forceinline__ int stage_tiles(int dtype, bool resid) {
   return n < kSampleStageMaxTiles ? n : kSampleStageMaxTiles;
 }
 
+template <bool SP>
 __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg, const float* q, int64_t ldq,
                                                                    const float* u_final, OutView out,
                                                                    CommitParams cp, Ws ws, int32_t excl_stride,
@@ -536,7 +589,7 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
         const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
         const ReqState rq = ws.state[b];
         if (!sampling_mode(rq.mode)) continue;
-        const bool resid = rq.mode == kModeResidual;
+        const bool resid = !SP && rq.mode == kModeResidual;
         const int per = stage_tiles(lg.dtype, resid);
         const int tc = min(tb, full_tiles);
         const int64_t row = rq.sample_row;
@@ -578,14 +631,17 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
     const ReqState rq = ws.state[b];
     if (!sampling_mode(rq.mode)) continue;
-    const bool resid = rq.mode == kModeResidual;
+    const bool resid = !SP && rq.mode == kModeResidual;
     const int per = stage_tiles(lg.dtype, resid);
     const int tc = min(tb, full_tiles);
     const int64_t row = rq.sample_row;
     const RowStat rs = ws.rowstat[row];
     const float inv_z = inverse_z(rs);
     const float u = u_final[b];
-    const int32_t* excl = ws.excl + static_cast<int64_t>(b) * excl_stride;
+    const bool sparse = SP && rq.mode == kModeResidualSparse;
+    const int32_t* excl = sparse ? ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap
+                                 : ws.excl + static_cast<int64_t>(b) * excl_stride;
+    const float* excl_q = sparse ? ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap : nullptr;
     uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
     for (int c0 = ta; c0 < tc; c0 += per, ++g) {
       const int n = min(per, tc - c0);
@@ -607,8 +663,9 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
           }
           float x[8], qv[8], w[8];
           lane_unpack(r, lg.dtype, resid, x, qv);
-          weights_from_values(x, qv, rs, inv_z, rq.mode, excl, rq.n_excl,
-                              static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+          weights_from_values<SP>(x, qv, rs, inv_z, sparse ? kModeP : rq.mode, excl, excl_q, rq.n_excl,
+                                  static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+          if (SP && sparse) apply_candidates_tile(w, static_cast<int64_t>(c0 + i) * kTile, lane, excl, excl_q, rq.n_excl);
           const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
           if (lane == 0) ts[c0 + i] = fx;
         }
@@ -618,8 +675,8 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     }
     for (int tile = max(tc, ta) + warp; tile < tb; tile += kSampleWarps) {  // the ragged last tile
       float w[8];
-      lane_weights(lg, q, ldq, row, rs, inv_z, rq.mode, excl, rq.n_excl, static_cast<int64_t>(tile) * kTile + lane * 8,
-                   w);
+      lane_weights<SP>(lg, q, ldq, row, rs, inv_z, rq.mode, excl, excl_q, rq.n_excl,
+                   static_cast<int64_t>(tile) * kTile + lane * 8, w);
       const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
       if (lane == 0) ts[tile] = fx;
     }
@@ -630,7 +687,7 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     }
     named_sync(kSampleThreads);
     if (ring.last) {
-      block_draw<true>(lg, q, ldq, u, out, cp, ws, excl_stride, static_cast<int>(b), rq, rs);
+      block_draw<true, SP>(lg, q, ldq, u, out, cp, ws, excl_stride, static_cast<int>(b), rq, rs);
       if (threadIdx.x == 0) ws.chunk_cnt[b] = 0u;  // leave the counter clean for the next call
       named_sync(kSampleThreads);
     }
@@ -646,21 +703,24 @@ __global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitPa
 }  // namespace
 
 cudaError_t sample_smem_setup() {
-  return cudaFuncSetAttribute(k_sample, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(k_sample<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kSampleSmemBytes));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_sample<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSampleSmemBytes));
 }
 
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
-                                     const DeviceInfo& dev, cudaStream_t stream) {
+                                     const DeviceInfo& dev, cudaStream_t stream, bool sparse_q) {
   // one resident wave (two blocks per SM, one slot for the commit block), at least ~16 tiles per block
   const int64_t tiles = static_cast<int64_t>(cp.batch) * ws.ntiles;
   int64_t nblocks = static_cast<int64_t>(dev.sms) * 2 - 1;
   if (nblocks > (tiles + 15) / 16) nblocks = (tiles + 15) / 16;
   if (nblocks < 1) nblocks = 1;
-  return launch_pdl(k_sample, dim3(static_cast<unsigned>(nblocks + 1)), dim3(kSampleBlockThreads), kSampleSmemBytes,
-                    stream, lg, q, ldq, u_final, out, cp, ws, static_cast<int32_t>(cp.max_len),
-                    static_cast<int32_t>(nblocks));
+  return launch_pdl(sparse_q ? k_sample<true> : k_sample<false>, dim3(static_cast<unsigned>(nblocks + 1)),
+                    dim3(kSampleBlockThreads), kSampleSmemBytes, stream, lg, q, ldq, u_final, out, cp, ws,
+                    static_cast<int32_t>(cp.max_len), static_cast<int32_t>(nblocks));
 }
 
 cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream) {

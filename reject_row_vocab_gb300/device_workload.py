@@ -13,8 +13,8 @@ import torch
 from . import specverify as sv
 from .workload import Workload
 
-_ARRAYS = ("cu_seqlens", "verify_ids", "q", "temperature", "u_accept", "u_final", "tokens", "parents",
-           "first_child", "next_sibling", "row_slots", "seq_lens")
+_ARRAYS = ("cu_seqlens", "verify_ids", "q", "cand_ids", "cand_probs", "temperature", "u_accept", "u_final",
+           "tokens", "parents", "first_child", "next_sibling", "row_slots", "seq_lens")
 
 
 def padded_rows(t: torch.Tensor, device) -> torch.Tensor:
@@ -88,6 +88,9 @@ def run(w: Workload, d: DeviceInputs, out: Optional[sv.VerifyOutputs] = None, ws
     if w.kind == "rejection_chain":
         return sv.rejection_chain(d["logits"], d["verify_ids"], w.max_len - 1, d["q"], d["temperature"],
                                   d["u_accept"], d["u_final"], **kw)
+    if w.kind == "rejection_chain_sparse":
+        return sv.rejection_chain_sparse(d["logits"], d["verify_ids"], w.max_len - 1, d["cand_ids"], d["cand_probs"],
+                                         d["temperature"], d["u_accept"], d["u_final"], **kw)
     if w.kind == "rejection_ragged":
         return sv.rejection_ragged(d["logits"], d["cu_seqlens"], w.max_len, d["verify_ids"], d["q"],
                                    d["temperature"], d["u_accept"], d["u_final"], **kw)
@@ -102,6 +105,8 @@ def run(w: Workload, d: DeviceInputs, out: Optional[sv.VerifyOutputs] = None, ws
 
 
 def workspace_for(w: Workload, device="cuda") -> torch.Tensor:
+    if w.cand_ids is not None:
+        return sv.sparse_workspace(w.rows, w.batch, w.vocab, kind_max_len(w), w.cand_ids.shape[1], device)
     return sv.workspace(w.rows, w.batch, w.vocab, kind_max_len(w), device)
 
 

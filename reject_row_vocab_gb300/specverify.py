@@ -28,7 +28,8 @@ ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spe
                 "spec_verify_greedy_tree", "spec_verify_rejection_chain", "spec_verify_rejection_ragged",
                 "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events",
                 "spec_verify_last_cuda_error", "spec_verify_rejection_chain_noalloc",
-                "spec_verify_dspark_workspace_bytes", "spec_verify_dspark_budget", "spec_verify_dspark_verify_lens")
+                "spec_verify_dspark_workspace_bytes", "spec_verify_dspark_budget", "spec_verify_dspark_verify_lens",
+                "spec_verify_sparse_workspace_bytes", "spec_verify_rejection_chain_sparse")
 
 
 class SpecVerifyError(RuntimeError):
@@ -71,6 +72,9 @@ def load_library():
                                           OUT, P, SZ, P], ctypes.c_int),
         "spec_verify_row_stats": ([P, ctypes.c_int, I64, I64, I32, P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
         "spec_verify_set_stats_events": ([P, P], ctypes.c_int),
+        "spec_verify_sparse_workspace_bytes": ([I64, I32, I32, I32, I32], SZ),
+        "spec_verify_rejection_chain_sparse": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, I32, I64, P, P, P, P, P,
+                                                OUT, P, SZ, P], ctypes.c_int),
         "spec_verify_dspark_workspace_bytes": ([I32], SZ),
         "spec_verify_dspark_budget": ([P, I64, I32, P, I32, F, P], ctypes.c_int),
         "spec_verify_dspark_verify_lens": ([P, I32, I32, I64, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
@@ -197,6 +201,30 @@ def rejection_chain(logits, verify_ids, m, q, temperature, u_accept, u_final, *,
         _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(q), q.stride(0),
         _ptr(temperature), _ptr(u_accept), _ptr(u_final), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def sparse_workspace(rows: int, batch: int, vocab: int, max_len: int, num_cands: int, device=None) -> torch.Tensor:
+    lib = load_library()
+    n = int(lib.spec_verify_sparse_workspace_bytes(rows, batch, vocab, max_len, num_cands))
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def rejection_chain_sparse(logits, verify_ids, m, cand_ids, cand_probs, temperature, u_accept, u_final, *,
+                           row_slots=None, seq_lens=None, out=None, ws=None, stream=None):
+    """p/q rejection chain whose q is given by candidate lists cand_ids / cand_probs [rows, K]."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch = rows // (m + 1)
+    K = cand_ids.shape[1]
+    if ws is None:
+        ws = sparse_workspace(rows, batch, V, m + 1, K, logits.device)
+    out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_rejection_chain_sparse", lib.spec_verify_rejection_chain_sparse(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(cand_ids),
+        _ptr(cand_probs), K, cand_ids.stride(0), _ptr(temperature), _ptr(u_accept), _ptr(u_final),
+        _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 
