@@ -289,6 +289,32 @@ sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t 
  * min_len < 1, max_len < min_len, R * D > 2^30; SV_ERR_WORKSPACE_TOO_SMALL)
  * return before anything is enqueued.
  */
+/*
+ * Tree-verify inputs from parent lists ([E2D] §2.4: a flattened tree where each
+ * node sees the committed history, its ancestors and itself, with position ids
+ * from the path depth; §3.4: tree construction produces the mask, positions
+ * and the retrieve index / next-token / next-sibling arrays of the verify walk).
+ * parents [batch, nodes] (device int32): node 0 is the root (parent -1), every
+ * other node's parent has a smaller index.  seq_lens [batch] (device int64,
+ * may be NULL for 0): the committed length before the tree.  Outputs, all
+ * device, caller-owned:
+ *   positions      [batch, nodes] int64  seq_len + depth
+ *   mask           [batch, nodes, nodes] uint8, mask[b][i][j] = 1 iff node j
+ *                  is node i or one of its ancestors
+ *   retrieve_index [batch, nodes] int32  b * nodes + i
+ *   first_child    [batch, nodes] int32  lowest-index child, -1 if none
+ *   next_sibling   [batch, nodes] int32  next higher-index node with the same
+ *                  parent, -1 if none (the format the tree entry points accept)
+ *   status         [batch] uint32        SV_DEV_BAD_TREE for an invalid parent
+ *                  array (its outputs: depth 0, identity mask, -1 links)
+ * 1 <= nodes <= 1024, batch <= 65535; SV_ERR_BAD_SHAPE / SV_ERR_NULL_ARG
+ * before anything is enqueued.  No workspace.
+ */
+sv_status_t spec_verify_build_tree(const int32_t* parents, const int64_t* seq_lens, int32_t batch, int32_t nodes,
+                                   int64_t* positions, uint8_t* mask, int32_t* retrieve_index,
+                                   int32_t* first_child, int32_t* next_sibling, uint32_t* status,
+                                   cudaStream_t stream);
+
 size_t spec_verify_dspark_workspace_bytes(int32_t num_requests);
 
 sv_status_t spec_verify_dspark_budget(const float* hist_survival, int64_t n, int32_t num_requests, const float* sps,

@@ -89,6 +89,18 @@ __device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, boo
 
 // Weights of eight entries from their values; the single definition both
 // passes use, so a tile's weights are bit-identical in both.
+// A sparse residual row's first 32 candidates held in registers, one per
+// lane (loaded once per request; later entries are read from memory).
+struct CandRegs {
+  int32_t id;
+  float q;
+};
+
+__device__ __forceinline__ CandRegs load_cand_regs(const int32_t* cid, const float* cq, int32_t n) {
+  const int lane = threadIdx.x & 31;
+  return CandRegs{lane < n ? cid[lane] : -1, lane < n ? cq[lane] : 0.0f};
+}
+
 // SP: the kernel serves sparse-q requests (kModeResidualSparse); without it
 // that mode is compiled out.  For kModePExcl (excl, n_excl) lists the tokens to zero; for
 // kModeResidualSparse (excl, excl_q, n_excl) is the row's candidate list
@@ -98,7 +110,7 @@ template <bool SP>
 __device__ __forceinline__ void weights_from_values(const float (&x)[8], const float (&qv)[8], const RowStat& rs,
                                                     float inv_z, int32_t mode, const int32_t* excl,
                                                     const float* excl_q, int32_t n_excl, int64_t col0,
-                                                    float (&w)[8]) {
+                                                    float (&w)[8], const CandRegs& cr = CandRegs{-1, 0.0f}) {
   // Packed pairs: each lane of a pair rounds exactly like the scalar
   // operation, so w_i = fl(fl(ex2(fl(fl(x_i - M) * k)) / Z) - q_i) either way.
   const float2 nM = make_float2(-rs.M, -rs.M), kk = make_float2(rs.k, rs.k), iz = make_float2(inv_z, inv_z);
@@ -124,11 +136,12 @@ __device__ __forceinline__ void weights_from_values(const float (&x)[8], const f
       for (int i = 0; i < 8; ++i)
         if (d == i) w[i] = 0.0f;
     }
-  } else if (SP && mode == kModeResidualSparse) {
+  } else if (SP && mode == kModeResidualSparse) {  // whole warp: the first 32 entries come by shuffle
     for (int e = 0; e < n_excl; ++e) {
-      const int64_t d = static_cast<int64_t>(excl[e]) - col0;
+      const int32_t id = e < 32 ? __shfl_sync(0xffffffffu, cr.id, e) : excl[e];
+      const float qe = e < 32 ? __shfl_sync(0xffffffffu, cr.q, e) : excl_q[e];
+      const int64_t d = static_cast<int64_t>(id) - col0;
       if (d >= 0 && d < 8) {
-        const float qe = excl_q[e];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if (d == i) w[i] = __fsub_rn(w[i], qe);
@@ -144,11 +157,11 @@ __device__ __forceinline__ void weights_from_values(const float (&x)[8], const f
 // owning lane subtracts them, in list order, so the result equals the lane
 // loop of weights_from_values exactly.  w holds p on entry.
 __device__ __forceinline__ void apply_candidates_tile(float (&w)[8], int64_t t0, int lane, const int32_t* cid,
-                                                      const float* cq, int32_t n) {
+                                                      const float* cq, int32_t n, const CandRegs& cr) {
   for (int g = 0; g < n; g += 32) {
     const int c = g + lane;
-    const int32_t id = c < n ? cid[c] : -1;
-    const float qq = c < n ? cq[c] : 0.0f;
+    const int32_t id = g == 0 ? cr.id : (c < n ? cid[c] : -1);
+    const float qq = g == 0 ? cr.q : (c < n ? cq[c] : 0.0f);
     const int64_t off = static_cast<int64_t>(id) - t0;
     unsigned hit = __ballot_sync(0xffffffffu, c < n && off >= 0 && off < kTile);
     while (hit) {
@@ -172,7 +185,8 @@ __device__ __forceinline__ void apply_candidates_tile(float (&w)[8], int64_t t0,
 template <bool SP>
 __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
                                              const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
-                                             const float* excl_q, int32_t n_excl, int64_t col0, float (&w)[8]) {
+                                             const float* excl_q, int32_t n_excl, int64_t col0, float (&w)[8],
+                                             const CandRegs& cr = CandRegs{-1, 0.0f}) {
   const bool resid = !SP && mode == kModeResidual;  // a sparse-q kernel never reads dense q
   float x[8], qv[8];
   if (col0 + 8 <= lg.vocab) {
@@ -187,7 +201,7 @@ __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* 
       qv[i] = (resid && in) ? __ldg(q + row * ldq + col0 + i) : 0.0f;
     }
   }
-  weights_from_values<SP>(x, qv, rs, inv_z, mode, excl, excl_q, n_excl, col0, w);
+  weights_from_values<SP>(x, qv, rs, inv_z, mode, excl, excl_q, n_excl, col0, w, cr);
 }
 
 // A lane's weight sum: fp32, left to right.  Pass B walks the same additions.
@@ -478,8 +492,10 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
     const uint64_t tpre = located ? s_pre : 0;
     const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
     float w[8];
+    const CandRegs cr = (SP && mode == kModeResidualSparse) ? load_cand_regs(excl, excl_q, rq.n_excl)
+                                                            : CandRegs{-1, 0.0f};
     lane_weights<SP>(lg, q, ldq, row, rs, inv_z, mode, excl, excl_q,
-                 (mode == kModePExcl || mode == kModeResidualSparse) ? rq.n_excl : 0, col0, w);
+                     (mode == kModePExcl || mode == kModeResidualSparse) ? rq.n_excl : 0, col0, w, cr);
     const uint64_t W = to_fixed(lane_sum(w));
     const uint64_t li = warp_inclusive_scan_u64(W);
     const uint64_t lo = tpre + (li - W), hi = tpre + li;
@@ -637,11 +653,11 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     const int64_t row = rq.sample_row;
     const RowStat rs = ws.rowstat[row];
     const float inv_z = inverse_z(rs);
-    const float u = u_final[b];
     const bool sparse = SP && rq.mode == kModeResidualSparse;
     const int32_t* excl = sparse ? ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap
                                  : ws.excl + static_cast<int64_t>(b) * excl_stride;
     const float* excl_q = sparse ? ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap : nullptr;
+    const CandRegs cr = sparse ? load_cand_regs(excl, excl_q, rq.n_excl) : CandRegs{-1, 0.0f};
     uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
     for (int c0 = ta; c0 < tc; c0 += per, ++g) {
       const int n = min(per, tc - c0);
@@ -652,7 +668,10 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
         ring.abort = 1;
         atomicOr(ws.err, 1u);
       } else {
-        for (int i = warp; i < n; i += kSampleWarps) {
+        // Sparse q: two tiles per warp and iteration, so their dependency
+        // chains (weights, lane sum, fixed-point conversion, warp reduction)
+        // overlap.
+        auto tile_sum = [&](int i) -> uint64_t {
           const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
           LaneRaw r;
           r.l0 = lds16(smem_addr(src) + off * es);
@@ -665,9 +684,27 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
           lane_unpack(r, lg.dtype, resid, x, qv);
           weights_from_values<SP>(x, qv, rs, inv_z, sparse ? kModeP : rq.mode, excl, excl_q, rq.n_excl,
                                   static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
-          if (SP && sparse) apply_candidates_tile(w, static_cast<int64_t>(c0 + i) * kTile, lane, excl, excl_q, rq.n_excl);
-          const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
-          if (lane == 0) ts[c0 + i] = fx;
+          if (SP && sparse)
+            apply_candidates_tile(w, static_cast<int64_t>(c0 + i) * kTile, lane, excl, excl_q, rq.n_excl, cr);
+          return to_fixed(lane_sum(w));
+        };
+        if constexpr (SP) {
+          for (int i = warp; i < n; i += 2 * kSampleWarps) {
+            const int i2 = i + kSampleWarps;
+            const uint64_t a = tile_sum(i);
+            const uint64_t c = i2 < n ? tile_sum(i2) : 0ull;  // i2 < n is the same in every lane
+            const uint64_t fa = warp_sum_u64(a);
+            const uint64_t fc = warp_sum_u64(c);
+            if (lane == 0) {
+              ts[c0 + i] = fa;
+              if (i2 < n) ts[c0 + i2] = fc;
+            }
+          }
+        } else {  // dense q: the q loads already fill the registers; one tile at a time
+          for (int i = warp; i < n; i += kSampleWarps) {
+            const uint64_t fa = warp_sum_u64(tile_sum(i));
+            if (lane == 0) ts[c0 + i] = fa;
+          }
         }
       }
       __syncwarp();
@@ -676,22 +713,27 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
     for (int tile = max(tc, ta) + warp; tile < tb; tile += kSampleWarps) {  // the ragged last tile
       float w[8];
       lane_weights<SP>(lg, q, ldq, row, rs, inv_z, rq.mode, excl, excl_q, rq.n_excl,
-                   static_cast<int64_t>(tile) * kTile + lane * 8, w);
+                       static_cast<int64_t>(tile) * kTile + lane * 8, w, cr);
       const uint64_t fx = warp_sum_u64(to_fixed(lane_sum(w)));
       if (lane == 0) ts[tile] = fx;
     }
-    named_sync(kSampleThreads);
-    if (threadIdx.x == 0) {
-      const unsigned add = static_cast<unsigned>(tb - ta);
-      ring.last = (ticket_add(&ws.chunk_cnt[b], add) + add == static_cast<unsigned>(T));
-    }
-    named_sync(kSampleThreads);
-    if (ring.last) {
-      block_draw<true, SP>(lg, q, ldq, u, out, cp, ws, excl_stride, static_cast<int>(b), rq, rs);
-      if (threadIdx.x == 0) ws.chunk_cnt[b] = 0u;  // leave the counter clean for the next call
-      named_sync(kSampleThreads);
-    }
   }
+}
+
+// The draws, one CTA per request, once every tile sum exists (this grid
+// starts after k_sample has completed): no streaming block ever stops to
+// draw, and all requests draw at the same time.
+template <bool SP>
+__global__ void __launch_bounds__(kSampleThreads) k_draw(LogitsView lg, const float* q, int64_t ldq,
+                                                         const float* u_final, OutView out, CommitParams cp, Ws ws,
+                                                         int32_t excl_stride) {
+  grid_dependency_wait();  // the tile sums of k_sample
+  allow_dependents();
+  const int b = blockIdx.x;
+  const ReqState rq = ws.state[b];
+  if (!sampling_mode(rq.mode)) return;
+  const RowStat rs = ws.rowstat[rq.sample_row];
+  block_draw<false, SP>(lg, q, ldq, u_final[b], out, cp, ws, excl_stride, b, rq, rs);
 }
 
 __global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitParams cp) {
@@ -718,9 +760,14 @@ cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64
   int64_t nblocks = static_cast<int64_t>(dev.sms) * 2 - 1;
   if (nblocks > (tiles + 15) / 16) nblocks = (tiles + 15) / 16;
   if (nblocks < 1) nblocks = 1;
-  return launch_pdl(sparse_q ? k_sample<true> : k_sample<false>, dim3(static_cast<unsigned>(nblocks + 1)),
-                    dim3(kSampleBlockThreads), kSampleSmemBytes, stream, lg, q, ldq, u_final, out, cp, ws,
-                    static_cast<int32_t>(cp.max_len), static_cast<int32_t>(nblocks));
+  const cudaError_t e =
+      launch_pdl(sparse_q ? k_sample<true> : k_sample<false>, dim3(static_cast<unsigned>(nblocks + 1)),
+                 dim3(kSampleBlockThreads), kSampleSmemBytes, stream, lg, q, ldq, u_final, out, cp, ws,
+                 static_cast<int32_t>(cp.max_len), static_cast<int32_t>(nblocks));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(sparse_q ? k_draw<true> : k_draw<false>, dim3(static_cast<unsigned>(cp.batch)),
+                    dim3(kSampleThreads), 0, stream, lg, q, ldq, u_final, out, cp, ws,
+                    static_cast<int32_t>(cp.max_len));
 }
 
 cudaError_t launch_commit(const OutView& out, const CommitParams& cp, cudaStream_t stream) {

@@ -29,7 +29,7 @@ ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spe
                 "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events",
                 "spec_verify_last_cuda_error", "spec_verify_rejection_chain_noalloc",
                 "spec_verify_dspark_workspace_bytes", "spec_verify_dspark_budget", "spec_verify_dspark_verify_lens",
-                "spec_verify_sparse_workspace_bytes", "spec_verify_rejection_chain_sparse")
+                "spec_verify_sparse_workspace_bytes", "spec_verify_rejection_chain_sparse", "spec_verify_build_tree")
 
 
 class SpecVerifyError(RuntimeError):
@@ -75,6 +75,7 @@ def load_library():
         "spec_verify_sparse_workspace_bytes": ([I64, I32, I32, I32, I32], SZ),
         "spec_verify_rejection_chain_sparse": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, I32, I64, P, P, P, P, P,
                                                 OUT, P, SZ, P], ctypes.c_int),
+        "spec_verify_build_tree": ([P, P, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
         "spec_verify_dspark_workspace_bytes": ([I32], SZ),
         "spec_verify_dspark_budget": ([P, I64, I32, P, I32, F, P], ctypes.c_int),
         "spec_verify_dspark_verify_lens": ([P, I32, I32, I64, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
@@ -327,3 +328,20 @@ def dspark_verify_lens(survival, budget: int, *, min_len: int = 1, max_len: Opti
         _ptr(survival), R, D, survival.stride(0), int(budget), int(min_len), int(max_len), float(eps), _ptr(out),
         _ptr(ws), ws.numel(), _stream(stream)))
     return out
+
+
+def build_tree(parents, seq_lens=None, stream=None) -> dict:
+    """Positions, ancestor mask, retrieve index and child / sibling links from parents [B, N] (int32, device)."""
+    lib = load_library()
+    B, N = parents.shape
+    d = parents.device
+    res = {"positions": torch.empty(B, N, dtype=torch.int64, device=d),
+           "mask": torch.empty(B, N, N, dtype=torch.uint8, device=d),
+           "retrieve_index": torch.empty(B, N, dtype=torch.int32, device=d),
+           "first_child": torch.empty(B, N, dtype=torch.int32, device=d),
+           "next_sibling": torch.empty(B, N, dtype=torch.int32, device=d),
+           "status": torch.empty(B, dtype=torch.int32, device=d)}
+    _check("spec_verify_build_tree", lib.spec_verify_build_tree(
+        _ptr(parents), _ptr(seq_lens), B, N, _ptr(res["positions"]), _ptr(res["mask"]), _ptr(res["retrieve_index"]),
+        _ptr(res["first_child"]), _ptr(res["next_sibling"]), _ptr(res["status"]), _stream(stream)))
+    return res
