@@ -33,7 +33,7 @@ UNIT = "rows/s"
 # statistics, row merge, acceptance, then the commit alone (greedy) or the sampler (with the
 # commit) and the draws
 KERNELS_PER_STEP = {"greedy_chain": 4, "greedy_tree": 4, "rejection_chain": 5, "rejection_ragged": 5,
-                    "target_only_tree": 5, "rejection_chain_sparse": 5}
+                    "target_only_tree": 5, "rejection_chain_sparse": 5, "sample_match_chain": 5}
 STATS_SOURCES = ("reject_row_vocab_gb300/csrc/sv_stats.cu", "reject_row_vocab_gb300/csrc/sv_device.cuh")
 
 
@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--eager", action="store_true", help="launch every step from Python instead of a CUDA graph")
     ap.add_argument("--graph-steps", type=int, default=100, help="steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--match", action="store_true",
+                    help="rejection-chain workloads verified by independent target sampling and prefix match")
     ap.add_argument("--q-cands", type=int, default=0,
                     help="rejection chains only: q given as K candidates per row (sparse) instead of dense rows")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -226,6 +228,12 @@ def make_workload(args, rank: int = 0):
         return wl.rejection_chain_sparse(vocab=151936, dtype="bf16", K=args.q_cands, sigma=3.0,
                                          seed=rank_seed(args.config, rank), **kw)
     kw = {"seed": rank_seed(args.config, rank)}
+    if args.match:
+        if args.config not in (2, 4):
+            raise SystemExit("--match applies to the rejection-chain workloads (2, 4)")
+        import dataclasses
+        w = wl.config(args.config, **kw)
+        return dataclasses.replace(w, kind="sample_match_chain", q=None, name=w.name + "_sample_match")
     if args.config == 3:
         kw["mode"] = args.tree_mode
     return wl.config(args.config, **kw)
@@ -247,6 +255,9 @@ def oracle_run(w, threads: int):
         return oracle.verify_chain(w, threads=threads)
     if w.kind == "rejection_chain_sparse":
         return oracle.verify_chain_sparse(w, threads=threads)
+    if w.kind == "sample_match_chain":
+        from oracle import match
+        return match.verify_chain_match(w)
     return oracle.verify_tree(w, "greedy" if w.kind == "greedy_tree" else "target_only", threads=threads)
 
 

@@ -161,6 +161,27 @@ sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, in
                                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Verification by independent target sampling and prefix match ([E2D] §1.2:
+ * a verification of its own, distinct from p/q rejection; the DFlash
+ * inference loop: sample the target's posterior at every block position, the
+ * accept length is the longest prefix where draft and sample agree, and the
+ * first mismatch emits the sample).  Same layout and outputs as
+ * spec_verify_rejection_chain, without q: row i's target token is drawn by
+ * inverse CDF with u_sample[i] (argmax for a greedy request), draft
+ * verify_ids[i + 1] is accepted iff it equals that draw, and the first
+ * rejected row (or the last row when every draft is accepted) emits its own
+ * draw.  No row is drawn in full except the one emitting: the statistics pass
+ * also sums each row's probabilities below its draft token, and the draw
+ * equals the draft iff u * Z lies in [that sum, that sum + p(draft) * Z).
+ * ws: spec_verify_workspace_bytes(batch * (m + 1), batch, vocab, m + 1) bytes.
+ */
+sv_status_t spec_verify_sample_match_chain(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                           int32_t m, int32_t vocab, const int32_t* verify_ids,
+                                           const float* temperature, const float* u_sample, const int64_t* row_slots,
+                                           const int64_t* seq_lens, const sv_out_t* out, void* ws, size_t ws_bytes,
+                                           cudaStream_t stream);
+
+/*
  * p/q rejection chain with a SPARSE q ([E2D] §6.2, §6.5: a candidate selector
  * proposes from K candidates; its q is zero outside them, and tokens outside
  * the candidates can still come out through the residual [p - q]_+).  Same

@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
       pre_d = d;
       if (!greedy && d >= 0 && d < p.lg.vocab) {
         pre_l = load_logit(p.lg, row, d);
-        if (!sparse) pre_q = p.q[row * p.ldq + d];
+        if (!sparse && !p.match) pre_q = p.q[row * p.ldq + d];
         pre_u = p.u_accept[row];
       }
     }
@@ -197,9 +197,18 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
       } else {
         bool unused = false;
         const float l = j0 == 0 ? pre_l : load_logit(p.lg, row, d);
-        const float qd = j0 == 0 ? pre_q : (sparse ? sparse_q_at(p, row, d, &unused) : p.q[row * p.ldq + d]);
         const float u = j0 == 0 ? pre_u : p.u_accept[row];
-        stop = (__fmul_rn(u, qd) < target_prob(l, rs)) ? 0 : 1;
+        if (p.match) {
+          // The target's own inverse-CDF draw with u equals d iff u * Z falls in
+          // [sum below d, sum below d + term of d) (all in Z's units).
+          const float uz = __fmul_rn(u, rs.Z);
+          const float ed = usable_logit(l) ? exp2f((l - rs.M) * rs.k) : 0.0f;
+          stop = (uz >= rs.below && uz < __fadd_rn(rs.below, ed)) ? 0 : 1;
+        } else {
+          const float qd =
+              j0 == 0 ? pre_q : (sparse ? sparse_q_at(p, row, d, &unused) : p.q[row * p.ldq + d]);
+          stop = (__fmul_rn(u, qd) < target_prob(l, rs)) ? 0 : 1;
+        }
       }
     }
     const unsigned bal = __ballot_sync(kFull, tested && stop != 0);
@@ -232,7 +241,8 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
   } else if (greedy) {
     bonus = fs.argmax;
   } else {
-    mode = (how == 1) ? (sparse ? kModeResidualSparse : kModeResidual) : kModeP;
+    // sample-then-match: the final row is drawn from its own p with its own uniform
+    mode = (how == 1 && !p.match) ? (sparse ? kModeResidualSparse : kModeResidual) : kModeP;
   }
   int32_t n_list = 0;
   if (mode == kModeResidualSparse)
@@ -256,6 +266,7 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
     out.bonus[b] = bonus;
     out.dev_status[b] = st;
     ws.state[b] = ReqState{static_cast<int32_t>(s), static_cast<int32_t>(fr), mode, bonus, st, n_list, 0, 0};
+    if (p.match) ws.ureq[b] = p.u_accept[fr];
   }
 }
 

@@ -83,6 +83,8 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   w->err = w->done_cnt + 1;
   w->rowstat = reinterpret_cast<RowStat*>(base + L.rowstat);
   w->partial = reinterpret_cast<RowPartial*>(base + L.partial);
+  w->psb = reinterpret_cast<float*>(base + L.psb);
+  w->ureq = reinterpret_cast<float*>(base + L.ureq);
   w->state = reinterpret_cast<ReqState*>(base + L.state);
   w->excl = reinterpret_cast<int32_t*>(base + L.excl);
   w->cand_id = reinterpret_cast<int32_t*>(base + L.cand);
@@ -114,10 +116,11 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
   return cudaEventRecord(ev, stream);
 }
 
-cudaError_t row_stats_timed(const LogitsView& lg, const RowMap& map, const Ws& w, int grid, cudaStream_t stream) {
+cudaError_t row_stats_timed(const LogitsView& lg, const RowMap& map, const Ws& w, int grid, cudaStream_t stream,
+                            const int32_t* probe = nullptr, int32_t probe_rpr = 0) {
   cudaError_t e;
   if (t_stats_start && (e = record_event(t_stats_start, stream)) != cudaSuccess) return e;
-  e = launch_row_stats(lg, map, w, grid, stream);
+  e = launch_row_stats(lg, map, w, grid, stream, probe, probe_rpr);
   if (e != cudaSuccess) return e;
   if (t_stats_stop) return record_event(t_stats_stop, stream);
   return cudaSuccess;
@@ -255,6 +258,34 @@ sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, in
   const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
   return rejection_common(logits, dtype, ld, batch, rows, m + 1, m + 1, vocab, nullptr, verify_ids, q, ldq,
                           temperature, u_accept, u_final, row_slots, seq_lens, out, ws, ws_bytes, stream);
+}
+
+sv_status_t spec_verify_sample_match_chain(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
+                                           int32_t m, int32_t vocab, const int32_t* verify_ids,
+                                           const float* temperature, const float* u_sample, const int64_t* row_slots,
+                                           const int64_t* seq_lens, const sv_out_t* out, void* ws, size_t ws_bytes,
+                                           cudaStream_t stream) {
+  if (batch < 0 || m < 0 || m >= (1 << 20) || batch > 65535) return SV_ERR_BAD_SHAPE;
+  if (batch == 0) return empty_batch(out, stream);
+  const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
+  SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
+  if (!verify_ids || !temperature || !u_sample) return SV_ERR_NULL_ARG;
+  SV_TRY(check_out(out, row_slots, seq_lens));
+  Ws w{};
+  SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, m + 1, &w));
+  DeviceInfo dev{};
+  SV_TRY_CUDA(device_info(&dev));
+  const LogitsView lg{logits, dtype, ld, rows, vocab};
+  const OutView ov = out_view(out);
+  // probe[row] = verify_ids[row + 1]: the draft each row tests (the last row of a request tests none)
+  SV_TRY_CUDA(row_stats_timed(lg, RowMap{kMapFixed, m + 1, batch, nullptr, temperature}, w, stats_grid(dev, lg),
+                              stream, verify_ids + 1, m + 1));
+  ChainParams p{lg,       batch,    m + 1,   m + 1,   nullptr, verify_ids, nullptr, 0,
+                temperature, u_sample, u_sample, nullptr, nullptr, 0,        0,       1};
+  SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
+  SV_TRY_CUDA(launch_sample_and_commit(lg, nullptr, 0, w.ureq, ov,
+                                       CommitParams{batch, m + 1, row_slots, seq_lens, w.err}, w, dev, stream));
+  return SV_OK;
 }
 
 size_t spec_verify_sparse_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len,

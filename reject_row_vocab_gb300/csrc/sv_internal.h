@@ -33,8 +33,10 @@ struct RowStat {
   uint32_t flags;
   float k;
   float inv_z;
+  float below;  // sum over ids below the row's probe token, in Z's units (probe-aware pass only)
+  int32_t pad;
 };
-static_assert(sizeof(RowStat) == 24, "RowStat layout");
+static_assert(sizeof(RowStat) == 32, "RowStat layout");
 
 // A CTA's partial statistics for the part of one row it scanned.
 struct RowPartial {
@@ -79,7 +81,7 @@ constexpr int kMaxNodes = 1024;
 
 struct WsLayout {
   size_t chunk_cnt, done_cnt, counters_end;
-  size_t rowstat, partial, state, excl, cand, tsum, total;
+  size_t rowstat, partial, psb, state, excl, cand, ureq, tsum, total;
   int32_t cand_cap;  // candidate-list entries per request (sparse q), at least 1
   int32_t ntiles;
 };
@@ -102,12 +104,16 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
     int64_t cpr = (nfull + 1023) / 1024;
     if (cpr < 1) cpr = 1;
     off = align_up(off + sizeof(RowPartial) * static_cast<size_t>(rows > 0 ? rows : 1) * static_cast<size_t>(cpr), 256);
+    L.psb = off;  // the probe chunk's partial sum below the probe token, one float per chunk
+    off = align_up(off + sizeof(float) * static_cast<size_t>(rows > 0 ? rows : 1) * static_cast<size_t>(cpr), 256);
   }
   L.state = off;
   off = align_up(off + sizeof(ReqState) * static_cast<size_t>(batch > 0 ? batch : 1), 256);
   L.excl = off;
   off = align_up(off + sizeof(int32_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
                            static_cast<size_t>(max_len > 0 ? max_len : 1), 256);
+  L.ureq = off;  // per request: the uniform of its final draw when it differs from u_final
+  off = align_up(off + sizeof(float) * static_cast<size_t>(batch > 0 ? batch : 1), 256);
   L.cand = off;  // per request: the residual row's candidates sorted by id (id, probability)
   L.cand_cap = num_cands > 0 ? num_cands : 1;
   off = align_up(off + 8 * static_cast<size_t>(batch > 0 ? batch : 1) * static_cast<size_t>(L.cand_cap), 256);
@@ -126,6 +132,8 @@ struct Ws {
   uint32_t* err;  // sticky error word: a bounded wait gave up (reported as SV_DEV_TIMEOUT)
   RowStat* rowstat;
   RowPartial* partial;
+  float* psb;   // probe-aware pass: per chunk, the sum below the probe token
+  float* ureq;  // per request: the uniform of the final draw (sample-then-match)
   ReqState* state;
   int32_t* excl;
   int32_t* cand_id;  // [B, cand_cap] sorted candidate ids of a sparse residual row
@@ -187,6 +195,7 @@ struct ChainParams {
   const float* cand_probs;    // [rows, ldc] their probabilities
   int32_t num_cands;
   int64_t ldc;
+  int32_t match;              // 1: verification by independent target sampling and prefix match
 };
 
 // Largest candidate list per row a sparse q may have.
@@ -245,7 +254,10 @@ struct DeviceInfo {
 cudaError_t device_info(DeviceInfo* info);
 
 // Launchers (each enqueues on `stream` and returns the launch error).
-cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream);
+// probe: when non-NULL, probe[row] is row's probe token (every row but the last of each block of probe_rpr
+// rows); the pass also leaves RowStat.below, the sum over ids below it.
+cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
+                             const int32_t* probe = nullptr, int32_t probe_rpr = 0);
 int stats_grid(const DeviceInfo& dev, const LogitsView& lg);
 cudaError_t stats_occupancy(int dtype, int* blocks_per_sm);
 

@@ -58,6 +58,7 @@ struct StageMeta {
   float ik;      // 1/k (0 for greedy rows)
   int32_t nst;   // stages in this chunk
   int32_t tail;  // 1: the row's ragged tail vector follows this chunk
+  int32_t probe; // probe-aware pass: the row's probe token when it lies in this chunk, else -1
 };
 
 // How rows are cut into chunks (queue items).  Head rows [0, rows_a) are cut
@@ -99,6 +100,7 @@ __device__ __forceinline__ void chunk_geometry(const ChunkPlan& P, int32_t item,
 // One chunk's per-warp partials, handed from the consumers to the finalizer.
 struct ChunkSlot {
   Part wpart[kConsumerWarps];
+  float wsb[kConsumerWarps];  // probe chunk: per-warp sums below the probe, at the warp maximum
   int32_t item;
   int32_t row;
   float k;
@@ -147,6 +149,7 @@ struct ThreadAcc {
   float R;
   float bound;   // logits >= bound move the reference (+inf for greedy rows)
   float2 s;
+  float sb;      // probe chunk only: the part of s over ids below the probe
 };
 
 constexpr float kRefSlack = 16.0f;  // terms stay <= 2^16 between reference moves
@@ -154,7 +157,7 @@ constexpr float kMinFinite = -3.402823466e38f;
 
 template <bool EXP>
 __device__ __forceinline__ ThreadAcc acc_init() {
-  return ThreadAcc{-kInfF, -1, 0u, 0.0f, EXP ? kMinFinite : kInfF, make_float2(0.0f, 0.0f)};
+  return ThreadAcc{-kInfF, -1, 0u, 0.0f, EXP ? kMinFinite : kInfF, make_float2(0.0f, 0.0f), 0.0f};
 }
 
 // Move the reference up to the finite logit v (rare path).
@@ -168,6 +171,7 @@ __device__ __forceinline__ void move_ref(ThreadAcc& a, float v, float k, float i
   const bool have = a.s.x != 0.0f || a.s.y != 0.0f;
   const float f = have ? exp2f(a.R - Rn) : 0.0f;
   a.s = __fmul2_rn(a.s, make_float2(f, f));
+  a.sb *= f;
   a.R = Rn;
   a.bound = (Rn + kRefSlack) * ik;
 }
@@ -284,6 +288,70 @@ __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t 
   if (EXP) a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
 }
 
+// Probe-aware folding (one chunk per row): as above, and the terms of ids
+// below the probe token d are also added to a.sb.
+template <int E>
+__device__ __forceinline__ void consume_dirty_probe(ThreadAcc& a, const float (&x)[E], int32_t vec, float k, float ik,
+                                                    int32_t d) {
+  for (int i = 0; i < E; ++i) {
+    const float v = usable_logit(x[i]) ? x[i] : -kInfF;
+    if (v > a.m) {
+      a.m = v;
+      a.vidx = vec;
+    }
+    if (v >= a.bound) move_ref(a, v, k, ik);
+    const float t = ex2_fast(fmaf(v, k, -a.R));
+    a.s.x += t;
+    if (vec * E + i < d) a.sb += t;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void consume_probe(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik,
+                                              int32_t d) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+  unpack<DT>(raw, x);
+  const float vmax = raw_max_nan<DT>(raw);
+  if (!(vmax < a.bound)) {
+    if (!(vmax < kInfF)) {
+      a.flags |= kStNonFinite;
+      consume_dirty_probe<E>(a, x, vec, k, ik, d);
+      return;
+    }
+    move_ref(a, vmax, k, ik);
+  }
+  a.vidx = vmax > a.m ? vec : a.vidx;
+  a.m = fmaxf(a.m, vmax);
+  const float2 kk = make_float2(k, k), nR = make_float2(-a.R, -a.R);
+  float t[E];
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    const float2 y = __ffma2_rn(make_float2(x[i], x[i + 1]), kk, nR);
+    t[i] = ex2_fast(y.x);
+    t[i + 1] = ex2_fast(y.y);
+  }
+  float tot = 0.0f, below = 0.0f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    tot += t[i];
+    if (vec * E + i < d) below += t[i];
+  }
+  a.s.x += tot;
+  a.sb += below;
+}
+
+template <int DT>
+__device__ __forceinline__ void fold_stage_probe(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k,
+                                                 float ik, int32_t d) {
+  constexpr int PER = kChunkVecs / kConsumers;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int vi = threadIdx.x + j * kConsumers;
+    if (vi < n) consume_probe<DT>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik, d);
+  }
+}
+
 // The row's ragged tail (vocab not a multiple of the vector width) as vector nfull, by one thread.
 template <int DT, bool EXP>
 __device__ __forceinline__ void fold_tail(ThreadAcc& a, const LogitsView& lg, int64_t row, int64_t nfull, float k,
@@ -297,6 +365,20 @@ __device__ __forceinline__ void fold_tail(ThreadAcc& a, const LogitsView& lg, in
     if (col < lg.vocab && !usable_logit(x[i])) a.flags |= kStNonFinite;
   }
   consume_dirty<E, EXP>(a, x, static_cast<int32_t>(nfull), k, ik);
+}
+
+template <int DT>
+__device__ __forceinline__ void fold_tail_probe(ThreadAcc& a, const LogitsView& lg, int64_t row, int64_t nfull, float k,
+                                                float ik, int32_t d) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int64_t col = nfull * E + i;
+    x[i] = col < lg.vocab ? load_logit(lg, row, col) : -kInfF;
+    if (col < lg.vocab && !usable_logit(x[i])) a.flags |= kStNonFinite;
+  }
+  consume_dirty_probe<E>(a, x, static_cast<int32_t>(nfull), k, ik, d);
 }
 
 // Fold the first n vectors of a stage (vectors c0.. of the row).  A full
@@ -421,6 +503,14 @@ __device__ __forceinline__ float row_temperature(const RowMap& map, int32_t row,
   return e < 0 ? 0.0f : map.temperature[e];
 }
 
+// The sum part of warp_combine alone (same rescaling, same butterfly).
+__device__ __forceinline__ float warp_sum_scaled(float s, float e) {
+  float sc = s != 0.0f ? (e == 0.0f ? s : s * exp2f(e)) : 0.0f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, off);
+  return sc;
+}
+
 // Merge chunk partial b into a (sums relative to each side's own maximum).
 __device__ __forceinline__ void chunk_merge(Part& a, const Part& b, float k) {
   const float M = fmaxf(a.m, b.m);
@@ -436,8 +526,12 @@ __device__ __forceinline__ void chunk_merge(Part& a, const Part& b, float k) {
   a = Part{M, sa + sb, v, a.flags | b.flags};
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan) {
+// PFX: probe-aware pass (each row's probe token probe[row], for every row but
+// the last of each block of probe_rpr rows): the chunk holding the probe also
+// sums the terms of the ids below it.
+template <int DT, bool PFX>
+__global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan,
+                                                                const int32_t* probe, int32_t probe_rpr) {
   using VT = VecTraits<DT>;
   constexpr int E = VT::E;
   const int64_t n_items = plan.n_items;
@@ -496,6 +590,11 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       }
     };
     float nk = 0.0f, nik = 0.0f;  // k and 1/k of the next chunk's row
+    int32_t nd = -1;              // probe token of the next chunk's row (probe-aware pass)
+    auto probe_of = [&](int32_t row) -> int32_t {
+      if (!PFX || probe_rpr <= 0 || row % probe_rpr == probe_rpr - 1) return -1;
+      return probe[row];
+    };
     bool have_k = false, ok = true;
     // Stream the chunk at queue position `pos`, then move to the position whose ticket is in `tk`.
     auto chunk_out = [&](unsigned& tk) {
@@ -510,6 +609,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       const int32_t nst = s1 - s0;
       const int32_t tail = (ragged && last) ? 1 : 0;
       float k = 0.0f, ik = 0.0f;
+      int32_t cprobe = -1;  // the probe token when it lies in this chunk
       for (int32_t s = 0; s < nst; ++s, ++g) {
         const int st = g % kStages;
         const int32_t c0 = cc0 + s * kChunkVecs;
@@ -536,14 +636,24 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) return;
             row_k_of(row, nk, nik);
+            nd = probe_of(row);
             have_k = true;
           }
           k = nk;  // first use of the prefetched values: after the copy is on its way
           ik = nik;
           asm volatile("mov.b32 %0, %0;" : "+f"(k));
+          if (PFX) {
+            int32_t d = nd;
+            asm volatile("mov.b32 %0, %0;" : "+r"(d));
+            if (d >= 0 && d < lg.vocab) {
+              const int64_t pv = d / E;  // the ragged tail is vector nfull and rides on the row's last chunk
+              const bool here = pv >= nfull ? last : (pv / kChunkVecs >= s0 && pv / kChunkVecs < s1);
+              if (here) cprobe = d;
+            }
+          }
         }
         if (lane == 0) {
-          sm.meta[st] = StageMeta{item, row, c0, n, k, ik, nst, tail};
+          sm.meta[st] = StageMeta{item, row, c0, n, k, ik, nst, tail, cprobe};
           mbar_arrive(smem_addr(&sm.full[st]));
         }
       }
@@ -554,6 +664,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         bool nlast;
         chunk_geometry(plan, static_cast<int32_t>(pos), nrow, ns0, ns1, nlast);
         row_k_of(nrow, nk, nik);
+        nd = probe_of(nrow);
       }
     };
     while (pos < n_items) {
@@ -570,7 +681,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       } else if (!*abort) {  // end marker
         const int st = g % kStages;
         if (mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
-          sm.meta[st] = StageMeta{-1, 0, 0, 0, 0.0f, 0.0f, 0, 0};
+          sm.meta[st] = StageMeta{-1, 0, 0, 0, 0.0f, 0.0f, 0, 0, -1};
           mbar_arrive(smem_addr(&sm.full[st]));
           ended = true;
         } else {
@@ -634,11 +745,14 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       const int32_t row = sm.slot[sl].row;
       const float k = sm.slot[sl].k;
       Part wp = lane < kConsumerWarps ? sm.slot[sl].wpart[lane] : part_identity();
+      const float wsb = (PFX && lane < kConsumerWarps) ? sm.slot[sl].wsb[lane] : 0.0f;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.pempty[sl]));  // the slot is free again
       if (item < 0) break;
       const float M = warp_max(wp.m);
+      const float sbc = PFX ? warp_sum_scaled(wsb, (wp.m - M) * k) : 0.0f;
       wp = warp_combine(M, wp.m, wp.s, (wp.m - M) * k, wp.idx, wp.flags);
+      if (PFX && lane == 0) ws.psb[item] = sbc;
       if (lane == 0) {
         // The chunk's argmax element, from the vector it lies in (just streamed, usually still in L2).
         const int32_t idx = resolve_index<DT>(lg, row, nfull, wp.idx, M);
@@ -651,7 +765,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
 
   // ---------------------------------------------------------------- consumers
   // Hand a chunk's warp partial (or the end mark, item < 0) to the finalizer.
-  auto hand_over = [&](uint32_t c, const Part& p, int32_t item, int32_t row, float k) -> bool {
+  auto hand_over = [&](uint32_t c, const Part& p, int32_t item, int32_t row, float k, float sbw) -> bool {
     const int sl = c % kSlots;
     if (!mbar_wait_bounded(smem_addr(&sm.pempty[sl]), ((c / kSlots) & 1u) ^ 1u, &sm.abort, kWaitLimitNs,
                            kConsumerNap)) {
@@ -661,6 +775,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
     }
     if (lane == 0) {
       sm.slot[sl].wpart[warp] = p;
+      if (PFX) sm.slot[sl].wsb[warp] = sbw;
       if (warp == 0) {
         sm.slot[sl].item = item;
         sm.slot[sl].row = row;
@@ -681,17 +796,23 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
     }
     StageMeta md = sm.meta[st];
     if (md.item < 0) {
-      hand_over(c, part_identity(), -1, 0, 0.0f);
+      hand_over(c, part_identity(), -1, 0, 0.0f, 0.0f);
       break;
     }
     const int32_t item = md.item, row = md.row, nst = md.nst, tail = md.tail;
+    const int32_t pd = PFX ? md.probe : -1;
     const float k = md.k, ik = md.ik;
     Part p;
+    float sbw = 0.0f;
     bool ok = true;
     if (k > 0.0f) {
       ThreadAcc a = acc_init<true>();  // one partial per chunk: independent of the schedule
       for (int32_t s = 0;; ++s) {
-        fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
+        if (PFX && pd >= 0) {
+          fold_stage_probe<DT>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik, pd);
+        } else {
+          fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.empty[st]));  // the stage goes back to the producer
         ++g;
@@ -703,10 +824,18 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         }
         md = sm.meta[st];
       }
-      if (tail && threadIdx.x == 0) fold_tail<DT, true>(a, lg, row, nfull, k, ik);
+      if (tail && threadIdx.x == 0) {
+        if (PFX && pd >= 0) {
+          fold_tail_probe<DT>(a, lg, row, nfull, k, ik, pd);
+        } else {
+          fold_tail<DT, true>(a, lg, row, nfull, k, ik);
+        }
+      }
       const float M = warp_max(a.m);
       // 2^(R - M k) rescales the lane's sum to the warp maximum (one rounding).
-      p = warp_combine(M, a.m, a.s.x + a.s.y, -fmaf(M, k, -a.R), a.vidx, a.flags);
+      const float e = -fmaf(M, k, -a.R);
+      if (PFX && pd >= 0) sbw = warp_sum_scaled(a.sb, e);
+      p = warp_combine(M, a.m, a.s.x + a.s.y, e, a.vidx, a.flags);
     } else {
       ThreadAcc a = acc_init<false>();
       for (int32_t s = 0;; ++s) {
@@ -731,16 +860,19 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       atomicOr(ws.err, 1u);
       break;
     }
-    if (!hand_over(c, p, item, row, k)) break;
+    if (!hand_over(c, p, item, row, k, sbw)) break;
   }
 }
 
 // Row statistics from the chunk partials, one warp per row: merge the row's
 // chunks in chunk order (lane l takes chunks l, l+32, ...; the result does not
 // depend on which CTA streamed which chunk; equal maxima keep the lowest
-// index), and rewind the chunk queue for the next call.
-template <int DT>
-__global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, Ws ws, ChunkPlan plan) {
+// index), and rewind the chunk queue for the next call.  PFX: also the sum
+// below the row's probe token: every chunk wholly below it plus the probe
+// chunk's own partial, each rescaled to the row maximum.
+template <int DT, bool PFX>
+__global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, Ws ws, ChunkPlan plan, const int32_t* probe,
+                                                   int32_t probe_rpr) {
   grid_dependency_wait();  // the partials come from k_row_stats
   allow_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) ws.done_cnt[2] = 0u;
@@ -755,8 +887,34 @@ __global__ void __launch_bounds__(256) k_row_merge(LogitsView lg, Ws ws, ChunkPl
   for (int j = lane; j < cnt; j += 32) chunk_merge(acc, load_partial_cg(&ws.partial[base + j]), k);
   const float M = warp_max(acc.m);
   const Part p = warp_combine(M, acc.m, acc.s, (acc.m - M) * k, acc.idx, acc.flags);
+  float below = 0.0f;
+  if (PFX && probe_rpr > 0 && row % probe_rpr != probe_rpr - 1 && k > 0.0f && M > -kInfF) {
+    const int32_t d = probe[row];
+    if (d >= 0 && d < lg.vocab) {
+      const int64_t nfull = lg.vocab / VecTraits<DT>::E;
+      const int64_t pv = d / VecTraits<DT>::E;
+      float part = 0.0f;  // this lane's chunks, in chunk order
+      for (int j = lane; j < cnt; j += 32) {
+        int32_t r, s0, s1;
+        bool last;
+        chunk_geometry(plan, static_cast<int32_t>(base + j), r, s0, s1, last);
+        const bool holds = pv >= nfull ? last : (pv / kChunkVecs >= s0 && pv / kChunkVecs < s1);
+        const bool wholly_below = !holds && static_cast<int64_t>(s1) * kChunkVecs <= pv;
+        if (holds || wholly_below) {
+          const Part c = load_partial_cg(&ws.partial[base + j]);
+          const float v = holds ? __ldcg(&ws.psb[base + j]) : c.s;
+          if (v != 0.0f) part += c.m == M ? v : v * exp2f((c.m - M) * k);
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+      below = part;
+    }
+  }
   if (lane == 0) {
     RowStat st;
+    st.below = below;
+    st.pad = 0;
     const bool samp = k > 0.0f && M > -kInfF;
     st.Z = samp ? p.s : 0.0f;
     st.inv_z = samp ? __fdiv_rn(1.0f, p.s) : 0.0f;
@@ -794,20 +952,20 @@ __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float
 
 }  // namespace
 
-cudaError_t stats_occupancy(int dtype, int* blocks_per_sm) {
-  cudaError_t e;
-  if (dtype == SV_BF16) {
-    e = cudaFuncSetAttribute(k_row_stats<SV_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kStatsSmemBytes));
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_BF16>, kStatsThreads,
-                                                         kStatsSmemBytes);
-  }
-  e = cudaFuncSetAttribute(k_row_stats<SV_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <int DT>
+cudaError_t stats_occupancy_t(int* blocks_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(k_row_stats<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kStatsSmemBytes));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_row_stats<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kStatsSmemBytes));
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<SV_F32>, kStatsThreads,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_row_stats<DT, false>, kStatsThreads,
                                                        kStatsSmemBytes);
+}
+
+cudaError_t stats_occupancy(int dtype, int* blocks_per_sm) {
+  return dtype == SV_BF16 ? stats_occupancy_t<SV_BF16>(blocks_per_sm) : stats_occupancy_t<SV_F32>(blocks_per_sm);
 }
 
 // Stages per row: 1024-vector pieces, at least one (the ragged tail rides on the last).
@@ -841,19 +999,26 @@ int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
   return static_cast<int>(g);
 }
 
-cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream) {
+template <int DT, bool PFX>
+cudaError_t launch_row_stats_t(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
+                               const ChunkPlan& plan, const int32_t* probe, int32_t probe_rpr) {
+  const dim3 mgrid(static_cast<unsigned>((lg.rows + 7) / 8));
+  const cudaError_t e = launch_pdl(k_row_stats<DT, PFX>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream,
+                                   lg, map, ws, plan, probe, probe_rpr);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_row_merge<DT, PFX>, mgrid, dim3(256), 0, stream, lg, ws, plan, probe, probe_rpr);
+}
+
+cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
+                             const int32_t* probe, int32_t probe_rpr) {
   const ChunkPlan plan = chunk_plan(lg, grid);
   if (plan.n_items > (int64_t{1} << 30)) return cudaErrorInvalidValue;  // chunk indices and the queue are 32-bit
-  const dim3 mgrid(static_cast<unsigned>((lg.rows + 7) / 8));
-  cudaError_t e;
   if (lg.dtype == SV_BF16) {
-    e = launch_pdl(k_row_stats<SV_BF16>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(k_row_merge<SV_BF16>, mgrid, dim3(256), 0, stream, lg, ws, plan);
+    return probe ? launch_row_stats_t<SV_BF16, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr)
+                 : launch_row_stats_t<SV_BF16, false>(lg, map, ws, grid, stream, plan, nullptr, 0);
   }
-  e = launch_pdl(k_row_stats<SV_F32>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map, ws, plan);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_row_merge<SV_F32>, mgrid, dim3(256), 0, stream, lg, ws, plan);
+  return probe ? launch_row_stats_t<SV_F32, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr)
+               : launch_row_stats_t<SV_F32, false>(lg, map, ws, grid, stream, plan, nullptr, 0);
 }
 
 cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,

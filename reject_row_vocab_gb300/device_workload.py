@@ -88,6 +88,8 @@ def run(w: Workload, d: DeviceInputs, out: Optional[sv.VerifyOutputs] = None, ws
     if w.kind == "rejection_chain":
         return sv.rejection_chain(d["logits"], d["verify_ids"], w.max_len - 1, d["q"], d["temperature"],
                                   d["u_accept"], d["u_final"], **kw)
+    if w.kind == "sample_match_chain":
+        return sv.sample_match_chain(d["logits"], d["verify_ids"], w.max_len - 1, d["temperature"], d["u_accept"], **kw)
     if w.kind == "rejection_chain_sparse":
         return sv.rejection_chain_sparse(d["logits"], d["verify_ids"], w.max_len - 1, d["cand_ids"], d["cand_probs"],
                                          d["temperature"], d["u_accept"], d["u_final"], **kw)

@@ -29,7 +29,8 @@ ENTRY_POINTS = ("spec_verify_workspace_bytes", "spec_verify_status_string", "spe
                 "spec_verify_target_only_tree", "spec_verify_row_stats", "spec_verify_set_stats_events",
                 "spec_verify_last_cuda_error", "spec_verify_rejection_chain_noalloc",
                 "spec_verify_dspark_workspace_bytes", "spec_verify_dspark_budget", "spec_verify_dspark_verify_lens",
-                "spec_verify_sparse_workspace_bytes", "spec_verify_rejection_chain_sparse", "spec_verify_build_tree")
+                "spec_verify_sparse_workspace_bytes", "spec_verify_rejection_chain_sparse", "spec_verify_build_tree",
+                "spec_verify_sample_match_chain")
 
 
 class SpecVerifyError(RuntimeError):
@@ -76,6 +77,8 @@ def load_library():
         "spec_verify_rejection_chain_sparse": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, I32, I64, P, P, P, P, P,
                                                 OUT, P, SZ, P], ctypes.c_int),
         "spec_verify_build_tree": ([P, P, I32, I32, P, P, P, P, P, P, P], ctypes.c_int),
+        "spec_verify_sample_match_chain": ([P, ctypes.c_int, I64, I32, I32, I32, P, P, P, P, P, OUT, P, SZ, P],
+                                           ctypes.c_int),
         "spec_verify_dspark_workspace_bytes": ([I32], SZ),
         "spec_verify_dspark_budget": ([P, I64, I32, P, I32, F, P], ctypes.c_int),
         "spec_verify_dspark_verify_lens": ([P, I32, I32, I64, I32, I32, I32, F, P, P, SZ, P], ctypes.c_int),
@@ -202,6 +205,20 @@ def rejection_chain(logits, verify_ids, m, q, temperature, u_accept, u_final, *,
         _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(q), q.stride(0),
         _ptr(temperature), _ptr(u_accept), _ptr(u_final), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def sample_match_chain(logits, verify_ids, m, temperature, u_sample, *, row_slots=None, seq_lens=None, out=None,
+                       ws=None, stream=None):
+    """Verification by independent target sampling (u_sample per row) and prefix match."""
+    lib = load_library()
+    rows, V = logits.shape
+    batch = rows // (m + 1)
+    out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
+    st = out.struct()
+    _check("spec_verify_sample_match_chain", lib.spec_verify_sample_match_chain(
+        _ptr(logits), _dtype(logits), logits.stride(0), batch, m, V, _ptr(verify_ids), _ptr(temperature),
+        _ptr(u_sample), _ptr(row_slots), _ptr(seq_lens), ctypes.byref(st), _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

@@ -51,7 +51,7 @@ def uniforms(rng: np.random.Generator, n: int) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 KINDS = ("greedy_chain", "rejection_chain", "rejection_ragged", "greedy_tree", "target_only_tree",
-         "rejection_chain_sparse")
+         "rejection_chain_sparse", "sample_match_chain")
 
 
 @dataclass

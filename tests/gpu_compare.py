@@ -22,6 +22,9 @@ def oracle_outputs(w, use_lists=False):
         return oracle.verify_chain(w, threads=threads)
     if w.kind == "rejection_chain_sparse":
         return oracle.verify_chain_sparse(w, threads=threads)
+    if w.kind == "sample_match_chain":
+        from oracle import match
+        return match.verify_chain_match(w)
     if w.kind == "greedy_tree":
         return oracle.verify_tree(w, "greedy", threads=threads, use_lists=use_lists)
     return oracle.verify_tree(w, "target_only", threads=threads, use_lists=use_lists)
