@@ -251,7 +251,8 @@ __device__ __forceinline__ float2 exp_sum(const float (&x)[E], float k, float R)
 
 // Fold E logits one at a time, NaN and +inf entries read as -inf (the caller
 // flags them).
-template <int E, bool EXP>
+// BELOW: the vectors lie wholly below the row's probe token: their terms also go to a.sb.
+template <int E, bool EXP, bool BELOW = false>
 __device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E], int32_t vec, float k, float ik) {
   for (int i = 0; i < E; ++i) {
     const float v = usable_logit(x[i]) ? x[i] : -kInfF;
@@ -261,14 +262,16 @@ __device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E],
     }
     if (EXP) {
       if (v >= a.bound) move_ref(a, v, k, ik);
-      a.s.x += ex2_fast(fmaf(v, k, -a.R));
+      const float t = ex2_fast(fmaf(v, k, -a.R));
+      a.s.x += t;
+      if (BELOW) a.sb += t;
     }
   }
 }
 
 // Fold one vector.  The common case (clean data, maximum below the bound) is
 // branch-free.
-template <int DT, bool EXP>
+template <int DT, bool EXP, bool BELOW = false>
 __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
   float x[E];
@@ -277,7 +280,7 @@ __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t 
   if (!(vmax < a.bound)) {  // NaN / +inf present, or the reference must move (rare)
     if (!(vmax < kInfF)) {
       a.flags |= kStNonFinite;
-      consume_dirty<E, EXP>(a, x, vec, k, ik);
+      consume_dirty<E, EXP, BELOW>(a, x, vec, k, ik);
       return;
     }
     if (EXP) move_ref(a, vmax, k, ik);
@@ -285,7 +288,11 @@ __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t 
   const bool raised = vmax > a.m;
   a.vidx = raised ? vec : a.vidx;
   a.m = fmaxf(a.m, vmax);
-  if (EXP) a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
+  if (EXP) {
+    const float2 es = exp_sum<E>(x, k, a.R);
+    a.s = __fadd2_rn(a.s, es);
+    if (BELOW) a.sb += es.x + es.y;
+  }
 }
 
 // Probe-aware folding (one chunk per row): as above, and the terms of ids
@@ -384,7 +391,7 @@ __device__ __forceinline__ void fold_tail_probe(ThreadAcc& a, const LogitsView& 
 // Fold the first n vectors of a stage (vectors c0.. of the row).  A full
 // stage takes the thread's four vectors together: one check of their maximum
 // against the bound covers all four, then maxima and sums run branch-free.
-template <int DT, bool EXP>
+template <int DT, bool EXP, bool BELOW = false>
 __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
   constexpr int PER = kChunkVecs / kConsumers;  // vectors per consumer thread per full stage
@@ -401,7 +408,7 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
     for (int j = 1; j < PER; ++j) smax = fmax_nan(smax, vm[j]);
     if (!(smax < a.bound)) {  // NaN / +inf, or the reference must move: vector by vector (rare)
 #pragma unroll
-      for (int j = 0; j < PER; ++j) consume<DT, EXP>(a, raw[j], c0 + t + j * kConsumers, k, ik);
+      for (int j = 0; j < PER; ++j) consume<DT, EXP, BELOW>(a, raw[j], c0 + t + j * kConsumers, k, ik);
       return;
     }
 #pragma unroll
@@ -414,14 +421,16 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
       for (int j = 0; j < PER; ++j) {
         float x[E];
         unpack<DT>(raw[j], x);
-        a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
+        const float2 es = exp_sum<E>(x, k, a.R);
+        a.s = __fadd2_rn(a.s, es);
+        if (BELOW) a.sb += es.x + es.y;
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
       const int vi = t + j * kConsumers;
-      if (vi < n) consume<DT, EXP>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik);
+      if (vi < n) consume<DT, EXP, BELOW>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik);
     }
   }
 }
@@ -808,7 +817,12 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
     if (k > 0.0f) {
       ThreadAcc a = acc_init<true>();  // one partial per chunk: independent of the schedule
       for (int32_t s = 0;; ++s) {
-        if (PFX && pd >= 0) {
+        // In the probe chunk only the stage holding the probe's vector goes
+        // vector by vector; stages wholly below it add their sums to sb too.
+        const int64_t pv = PFX && pd >= 0 ? pd / E : -1;
+        if (PFX && pd >= 0 && md.c0 + md.n <= pv) {
+          fold_stage<DT, true, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
+        } else if (PFX && pd >= 0 && md.c0 <= pv) {
           fold_stage_probe<DT>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik, pd);
         } else {
           fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
