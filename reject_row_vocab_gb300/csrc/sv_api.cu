@@ -78,7 +78,6 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   const WsLayout L = ws_layout(rows, batch, vocab, max_len, num_cands);
   if (!ws || ws_bytes < L.total || !aligned(ws, 256)) return SV_ERR_WORKSPACE_TOO_SMALL;
   char* base = static_cast<char*>(ws);
-  w->chunk_cnt = reinterpret_cast<uint32_t*>(base + L.chunk_cnt);
   w->done_cnt = reinterpret_cast<uint32_t*>(base + L.done_cnt);
   w->err = w->done_cnt + 1;
   w->rowstat = reinterpret_cast<RowStat*>(base + L.rowstat);

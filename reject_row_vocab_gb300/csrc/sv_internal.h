@@ -80,7 +80,7 @@ constexpr int kTile = 256;
 constexpr int kMaxNodes = 1024;
 
 struct WsLayout {
-  size_t chunk_cnt, done_cnt, counters_end;
+  size_t done_cnt, counters_end;
   size_t rowstat, partial, psb, state, excl, cand, ureq, tsum, total;
   int32_t cand_cap;  // candidate-list entries per request (sparse q), at least 1
   int32_t ntiles;
@@ -91,8 +91,6 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, int32_t num_cands = 0) {
   WsLayout L{};
   size_t off = 0;
-  L.chunk_cnt = off;
-  off += sizeof(uint32_t) * static_cast<size_t>(batch > 0 ? batch : 1);
   L.done_cnt = off;
   off += sizeof(uint32_t) * 4;
   L.counters_end = off = align_up(off, 256);
@@ -127,7 +125,6 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
 
 // Workspace pointers carved from the caller's buffer.
 struct Ws {
-  uint32_t* chunk_cnt;
   uint32_t* done_cnt;
   uint32_t* err;  // sticky error word: a bounded wait gave up (reported as SV_DEV_TIMEOUT)
   RowStat* rowstat;

@@ -5,14 +5,15 @@
 // bonus from p, §1.1; inverse CDF as in §6.2 sample_path()):
 //   w_v = max(0, p_v - q_v)          after a rejection,
 //   w_v = p_v                        bonus after every draft passed,
-//   w_v = p_v, children zeroed       target-only tree stop ([SGO]).
-// Pass A splits each sampled row into tiles of 256 entries (one warp, eight
-// entries per lane) spread over many CTAs and stores every tile's weight sum.
-// Pass B (one CTA per request) scans the tile sums, picks the tile holding
-// t = u_final * S, and one warp re-forms that tile's weights with exactly the
-// same arithmetic to find the entry.  The last CTA to finish then performs
-// the commit: exclusive scan of commit_lens and the KV slot / position lists
-// ([E2D] §5.6.6, §8.1; [SGO] "两个容易误解的工程细节").
+//   w_v = p_v, children zeroed       target-only tree stop ([SGO]),
+//   w_v = max(0, p_v - q_v), q sparse (a candidate list, [E2D] §6.5).
+// Pass A (k_sample) splits each sampled row into tiles of 256 entries (one
+// warp, eight entries per lane) spread over many CTAs and stores every tile's
+// weight sum; one extra block performs the commit: exclusive scan of
+// commit_lens and the KV slot / position lists ([E2D] §5.6.6, §8.1; [SGO]
+// "两个容易误解的工程细节").  Pass B (k_draw, one CTA per request) scans the
+// tile sums, picks the tile holding t = u_final * S, and one warp re-forms that
+// tile's weights with exactly the same arithmetic to find the entry.
 //
 //   [E2D] "从 EAGLE 到 DFlash 2：SGLang 与 SpecForge 的投机解码训练和推理"
 //   [SGO] SGLang speculative-decoding overview (zdszero.github.io)
@@ -87,8 +88,6 @@ __device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, boo
   }
 }
 
-// Weights of eight entries from their values; the single definition both
-// passes use, so a tile's weights are bit-identical in both.
 // A sparse residual row's first 32 candidates held in registers, one per
 // lane (loaded once per request; later entries are read from memory).
 struct CandRegs {
@@ -101,6 +100,8 @@ __device__ __forceinline__ CandRegs load_cand_regs(const int32_t* cid, const flo
   return CandRegs{lane < n ? cid[lane] : -1, lane < n ? cq[lane] : 0.0f};
 }
 
+// Weights of eight entries from their values; the single definition both
+// passes use, so a tile's weights are bit-identical in both.
 // SP: the kernel serves sparse-q requests (kModeResidualSparse); without it
 // that mode is compiled out.  For kModePExcl (excl, n_excl) lists the tokens to zero; for
 // kModeResidualSparse (excl, excl_q, n_excl) is the row's candidate list
@@ -535,15 +536,13 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   }
 }
 
-// Final token and commit.  The batch's (request, tile) space is split into
+// Tile sums and commit.  The batch's (request, tile) space is split into
 // equal contiguous ranges, one per block (one resident wave).  In each block a
-// producer warp streams the sampled rows' tiles (logits, and q for a
+// producer warp streams the sampled rows' tiles (logits, and q for a dense
 // residual) through a ring of shared-memory stages with bulk copies; eight
-// consumer warps sum the weights of every tile.  After its part of a request
-// the block takes a ticket on the request, and the block completing the
-// request draws its token while the producer keeps streaming.  One extra
-// block performs the commit (it needs only the acceptance results).  Every
-// wait is bounded; no block waits on another.
+// consumer warps sum the weights of every tile.  The draws follow in k_draw,
+// once every sum exists.  One extra block performs the commit (it needs only
+// the acceptance results).  Every wait is bounded; no block waits on another.
 constexpr int kSampleStages = 3;
 constexpr int kSampleStageBytes = 32 * 1024;
 constexpr int kSampleStageMaxTiles = 32;
@@ -554,7 +553,6 @@ constexpr size_t kSampleSmemBytes = static_cast<size_t>(kSampleStages) * kSample
 struct SampleRing {
   unsigned long long full[kSampleStages];
   unsigned long long empty[kSampleStages];
-  int last;
   int abort;
 };
 
