@@ -409,7 +409,7 @@ def run_ours(args):
         "logit_gbs_per_step": alg_bytes * launched / elapsed_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": stats_traffic(), "kernel": "k_row_stats",
-                     "timed_span": "k_row_stats + k_row_merge (events bracket both launches)",
+                     "timed_span": "k_row_stats alone (events recorded around its launch)",
                      "bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
         "clocks": clk, "gpu_launches": KERNELS_PER_STEP[w.kind] * launched,

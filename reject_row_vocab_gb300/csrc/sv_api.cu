@@ -105,24 +105,12 @@ sv_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ER
 thread_local cudaEvent_t t_stats_start = nullptr;
 thread_local cudaEvent_t t_stats_stop = nullptr;
 
-// While a stream is being captured into a graph, an external record becomes an
-// event node of the graph; otherwise a plain record.
-cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  const cudaError_t e = cudaStreamIsCapturing(stream, &cs);
-  if (e != cudaSuccess) return e;
-  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
-  return cudaEventRecord(ev, stream);
-}
 
 cudaError_t row_stats_timed(const LogitsView& lg, const RowMap& map, const Ws& w, int grid, cudaStream_t stream,
                             const int32_t* probe = nullptr, int32_t probe_rpr = 0) {
   cudaError_t e;
   if (t_stats_start && (e = record_event(t_stats_start, stream)) != cudaSuccess) return e;
-  e = launch_row_stats(lg, map, w, grid, stream, probe, probe_rpr);
-  if (e != cudaSuccess) return e;
-  if (t_stats_stop) return record_event(t_stats_stop, stream);
-  return cudaSuccess;
+  return launch_row_stats(lg, map, w, grid, stream, probe, probe_rpr, t_stats_stop);
 }
 
 // An empty batch commits nothing: commit_cu = [0].  Every other pointer may be NULL.
@@ -148,6 +136,16 @@ thread_local cudaError_t t_last_cuda_error = cudaSuccess;
   } while (0)
 
 }  // namespace
+
+// While a stream is being captured into a graph, an external record becomes an
+// event node of the graph; otherwise a plain record.
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal);
+  return cudaEventRecord(ev, stream);
+}
 
 sv_status_t cuda_failure(cudaError_t e) {
   t_last_cuda_error = e;

@@ -253,8 +253,14 @@ cudaError_t device_info(DeviceInfo* info);
 // Launchers (each enqueues on `stream` and returns the launch error).
 // probe: when non-NULL, probe[row] is row's probe token (every row but the last of each block of probe_rpr
 // rows); the pass also leaves RowStat.below, the sum over ids below it.
+// stats_done: when non-NULL, recorded on the stream between the streaming pass and the row merge
+// (benchmark instrumentation of the streaming kernel alone).
 cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
-                             const int32_t* probe = nullptr, int32_t probe_rpr = 0);
+                             const int32_t* probe = nullptr, int32_t probe_rpr = 0,
+                             cudaEvent_t stats_done = nullptr);
+
+// Records ev on stream (as an event node while the stream is being captured).
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream);
 int stats_grid(const DeviceInfo& dev, const LogitsView& lg);
 cudaError_t stats_occupancy(int dtype, int* blocks_per_sm);
 

@@ -1015,24 +1015,26 @@ int stats_grid(const DeviceInfo& dev, const LogitsView& lg) {
 
 template <int DT, bool PFX>
 cudaError_t launch_row_stats_t(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
-                               const ChunkPlan& plan, const int32_t* probe, int32_t probe_rpr) {
+                               const ChunkPlan& plan, const int32_t* probe, int32_t probe_rpr,
+                               cudaEvent_t stats_done) {
   const dim3 mgrid(static_cast<unsigned>((lg.rows + 7) / 8));
-  const cudaError_t e = launch_pdl(k_row_stats<DT, PFX>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream,
-                                   lg, map, ws, plan, probe, probe_rpr);
+  cudaError_t e = launch_pdl(k_row_stats<DT, PFX>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map,
+                             ws, plan, probe, probe_rpr);
   if (e != cudaSuccess) return e;
+  if (stats_done && (e = record_event(stats_done, stream)) != cudaSuccess) return e;
   return launch_pdl(k_row_merge<DT, PFX>, mgrid, dim3(256), 0, stream, lg, ws, plan, probe, probe_rpr);
 }
 
 cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& ws, int grid, cudaStream_t stream,
-                             const int32_t* probe, int32_t probe_rpr) {
+                             const int32_t* probe, int32_t probe_rpr, cudaEvent_t stats_done) {
   const ChunkPlan plan = chunk_plan(lg, grid);
   if (plan.n_items > (int64_t{1} << 30)) return cudaErrorInvalidValue;  // chunk indices and the queue are 32-bit
   if (lg.dtype == SV_BF16) {
-    return probe ? launch_row_stats_t<SV_BF16, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr)
-                 : launch_row_stats_t<SV_BF16, false>(lg, map, ws, grid, stream, plan, nullptr, 0);
+    return probe ? launch_row_stats_t<SV_BF16, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr, stats_done)
+                 : launch_row_stats_t<SV_BF16, false>(lg, map, ws, grid, stream, plan, nullptr, 0, stats_done);
   }
-  return probe ? launch_row_stats_t<SV_F32, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr)
-               : launch_row_stats_t<SV_F32, false>(lg, map, ws, grid, stream, plan, nullptr, 0);
+  return probe ? launch_row_stats_t<SV_F32, true>(lg, map, ws, grid, stream, plan, probe, probe_rpr, stats_done)
+               : launch_row_stats_t<SV_F32, false>(lg, map, ws, grid, stream, plan, nullptr, 0, stats_done);
 }
 
 cudaError_t launch_export_stats(const LogitsView& lg, const Ws& ws, const int32_t* probe, float* out_max,
