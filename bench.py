@@ -52,6 +52,9 @@ def parse_args(argv=None):
                     help="rejection-chain workloads verified by independent target sampling and prefix match")
     ap.add_argument("--q-cands", type=int, default=0,
                     help="rejection chains only: q given as K candidates per row (sparse) instead of dense rows")
+    ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
+                    help="write a buffer larger than L2 before every step (auto: when the logits are smaller "
+                         "than twice the L2); the step time then excludes the flushes")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-s", type=float, default=150.0)
@@ -199,13 +202,17 @@ def measured_peaks() -> tuple:
         return 6800.0, "fallback"
 
 
-def stats_traffic() -> float | None:
-    """dram bytes per row-statistics launch from the committed ncu summary, if the kernel is unchanged."""
+def stats_traffic(w) -> float | None:
+    """dram bytes per row-statistics launch from the committed ncu summary, if the kernel is unchanged and the
+    summary covers this workload's logits."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
+        return None
+    base = rec.get("workload_name")
+    if w.kind == "sample_match_chain" or not (w.name == base or w.name.startswith("%s_sparse_q" % base)):
         return None
     h = hashlib.sha256()
     for p in STATS_SOURCES:
@@ -239,11 +246,26 @@ def make_workload(args, rank: int = 0):
     return wl.config(args.config, **kw)
 
 
-def describe(w) -> dict:
+L2_BYTES = 129e6
+FLUSH_BYTES = 256 << 20  # about twice the L2
+
+
+def flush_wanted(args, w) -> bool:
+    if args.flush_l2 == "auto":
+        return w.logit_bytes() < 2 * L2_BYTES
+    return args.flush_l2 == "on"
+
+
+def describe(w, flush: bool) -> dict:
+    if flush:
+        l2 = ("L2 flushed before every step (a %d MB write, then a read of as much); the step time is the span of flush + step minus "
+              "that of the flushes alone, the row-statistics time its own events" % (FLUSH_BYTES >> 20))
+    elif w.logit_bytes() > L2_BYTES:
+        l2 = "inputs larger than L2 (%.0f MB of logits vs 129 MB L2)" % (w.logit_bytes() / 1e6)
+    else:
+        l2 = "inputs smaller than L2, not flushed: repeated steps may hit in L2"
     return {"workload": w.name, "kind": w.kind, "batch": w.batch, "rows": w.rows, "vocab": w.vocab,
-            "max_len": w.max_len, "logit_dtype": w.dtype, "logit_bytes": w.logit_bytes(),
-            "l2": "inputs larger than L2 (%.0f MB of logits vs 129 MB L2)" % (w.logit_bytes() / 1e6)
-            if w.logit_bytes() > 129e6 else "inputs smaller than L2: repeated steps may hit in L2",
+            "max_len": w.max_len, "logit_dtype": w.dtype, "logit_bytes": w.logit_bytes(), "l2": l2,
             "seed": w.meta.get("seed")}
 
 
@@ -297,9 +319,23 @@ def run_ours(args):
     ws = dw.workspace_for(w)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
+    flush = flush_wanted(args, w)
+    flush_buf = torch.empty(FLUSH_BYTES if flush else 0, dtype=torch.uint8, device="cuda")
+    flush_rd = torch.ones((FLUSH_BYTES if flush else 0) // 4, dtype=torch.float32, device="cuda")
+
+    def flush_l2():
+        # The write evicts the previous step's lines; the read then evicts the written (dirty) lines, so their
+        # write-back happens here and not inside the next step.
+        flush_buf.fill_(1)
+        flush_rd.sum()
+
+    def step():
+        if flush:
+            flush_l2()
+        dw.run(w, d, out=out, ws=ws)
 
     for _ in range(max(W, 3)):
-        dw.run(w, d, out=out, ws=ws)
+        step()
     torch.cuda.synchronize()
 
     ev_start = torch.cuda.Event(enable_timing=True)
@@ -322,6 +358,8 @@ def run_ours(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=cap):
             for k in range(G):
+                if flush:
+                    flush_l2()
                 sv.set_stats_events(*pairs[k])
                 dw.run(w, d, out=out, ws=ws)
             sv.set_stats_events(None, None)
@@ -338,6 +376,8 @@ def run_ours(args):
     ev_start.record(stream)
     if graph is None:
         for k in range(K):
+            if flush:
+                flush_l2()
             sv.set_stats_events(*pairs[k % P])
             dw.run(w, d, out=out, ws=ws)
         sv.set_stats_events(None, None)
@@ -355,6 +395,28 @@ def run_ours(args):
     clk = clocks.stop()
 
     elapsed_s = ev_start.elapsed_time(ev_end) / 1e3
+    if flush:  # the same number of flushes alone, launched the same way, comes off the span
+        fgraph = None
+        if graph is not None:
+            fgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(fgraph, stream=cap):
+                for _ in range(G):
+                    flush_l2()
+            torch.cuda.synchronize()
+            fgraph.replay()
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        if fgraph is None:
+            for _ in range(launched):
+                flush_l2()
+        else:
+            for _ in range(launched // G):
+                fgraph.replay()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        elapsed_s -= f0.elapsed_time(f1) / 1e3
     max_s = ranks.max(elapsed_s)
     avg_stats_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)  # last recording of each pair
 
@@ -403,12 +465,12 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": launched,
         "warmup": max(W, 3), "ms_per_step": 1e3 * max_s / launched, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(describe(w), launch="eager" if graph is None else "cuda graph of %d steps" % G,
+        "config": dict(describe(w, flush), launch="eager" if graph is None else "cuda graph of %d steps" % G,
                        parallelism="replicas x%d (independent batches)" % ranks.world),
         "committed_tokens_per_s": tokens, "mean_accept_len": float(res["accept_len"].mean()),
         "logit_gbs_per_step": alg_bytes * launched / elapsed_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": stats_traffic(), "kernel": "k_row_stats",
+                     "traffic": stats_traffic(w), "kernel": "k_row_stats",
                      "timed_span": "k_row_stats alone (events recorded around its launch)",
                      "bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
@@ -453,7 +515,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1e3 * el / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": dict(describe(w), parallelism="host cores"),
+        "dtype": "f64", "data": "synthetic", "config": dict(describe(w, flush_wanted(args, w)), parallelism="host cores"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
