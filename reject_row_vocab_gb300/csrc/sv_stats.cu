@@ -78,8 +78,8 @@ struct ChunkPlan {
 };
 
 // Row, stage range [s0, s1) and "last chunk of its row" of a queue item.
-__device__ __forceinline__ void chunk_geometry(const ChunkPlan& P, int32_t item, int32_t& row, int32_t& s0,
-                                               int32_t& s1, bool& last) {
+__host__ __device__ __forceinline__ void chunk_geometry(const ChunkPlan& P, int32_t item, int32_t& row, int32_t& s0,
+                                                        int32_t& s1, bool& last) {
   if (item < P.n_a) {
     row = item / P.cpr_a;
     const int32_t ci = item - row * P.cpr_a;

@@ -1,0 +1,39 @@
+"""Host-side pieces of bench.py: L2-flush choice, config text, traffic record gating (no GPU)."""
+import json
+import os
+import sys
+import types
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _w(name, kind, logit_bytes):
+    return types.SimpleNamespace(name=name, kind=kind, batch=1, rows=1, vocab=1, max_len=1, dtype="bf16",
+                                 meta={"seed": 1}, logit_bytes=lambda: logit_bytes)
+
+
+def test_flush_choice_follows_l2_size():
+    import bench
+    small, large = _w("c3_greedy_tree", "greedy_tree", 69_771_264), _w("c4_dflash_block", "rejection_chain",
+                                                                         311_164_928)
+    auto = bench.parse_args([])
+    assert bench.flush_wanted(auto, small) and not bench.flush_wanted(auto, large)
+    assert bench.flush_wanted(bench.parse_args(["--flush-l2", "on"]), large)
+    assert not bench.flush_wanted(bench.parse_args(["--flush-l2", "off"]), small)
+    assert bench.FLUSH_BYTES > 1.9 * bench.L2_BYTES
+    assert "flushed" in bench.describe(small, True)["l2"]
+    assert "larger than L2" in bench.describe(large, False)["l2"]
+    assert "not flushed" in bench.describe(small, False)["l2"]
+
+
+def test_traffic_record_applies_only_to_its_workload_and_source():
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    base = rec["workload_name"]
+    t = bench.stats_traffic(_w(base, "rejection_chain", 1))
+    assert t == rec["bytes_per_full_launch"]  # the committed record matches the committed kernel source
+    assert bench.stats_traffic(_w(base + "_sparse_q16", "rejection_chain_sparse", 1)) == t
+    assert bench.stats_traffic(_w(base + "_sample_match", "sample_match_chain", 1)) is None
+    assert bench.stats_traffic(_w("c3_greedy_tree", "greedy_tree", 1)) is None
