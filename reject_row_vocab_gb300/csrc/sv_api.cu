@@ -2,10 +2,13 @@
 // launch sequence of each entry point.  Nothing here reads device memory or
 // synchronises; every kernel is enqueued on the caller's stream.
 //
-// Launch sequences:
-//   greedy chain / tree:        row stats -> accept -> commit
-//   rejection chain / ragged:   row stats -> accept -> sample tiles -> sample finish + commit
-//   target-only tree:           row stats -> accept (tree walk) -> sample tiles -> sample finish + commit
+// Launch sequences (each kernel chained to the previous one by programmatic
+// dependent launch):
+//   greedy chain / tree:          row stats -> row merge -> accept -> commit
+//   rejection chain / ragged,
+//   sparse q, sample-then-match:  row stats -> row merge -> accept -> sample (tile sums; an extra block
+//                                 commits) -> draw
+//   target-only tree:             row stats -> row merge -> accept (tree walk) -> sample -> draw
 #include <cmath>
 #include <cstdint>
 #include <cstring>
