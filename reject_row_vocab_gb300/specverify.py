@@ -95,6 +95,77 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# Argument checks.  The library takes raw device pointers and cannot tell a
+# host pointer, a wrong element type or a short array from a good one, and the
+# kernels would then read or write outside the arrays.  Every tensor is checked
+# here before its pointer is passed: on the logits' device, of the element type
+# the call reads, densely laid out (2-D arrays may have a row stride), and at
+# least as large as the call reads.  None is passed on as NULL; whether an
+# argument may be NULL is the library's decision (it returns SV_ERR_NULL_ARG).
+
+
+def _require_cuda(t: torch.Tensor, name: str = "logits"):
+    """The call's leading 2-D array: a CUDA tensor with dense rows; its device is the call's device."""
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError("%s must be a 2-D torch tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (got %s): the library has no CPU path" % (name, t.device))
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("%s rows must be dense (stride 1 along a row)" % name)
+
+
+def _arg(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, numel: int, device) -> Optional[torch.Tensor]:
+    """A 1-D (or dense N-D) array argument of at least numel elements."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.device != device:
+        raise ValueError("%s is on %s; the call runs on %s (the logits' device)" % (name, t.device, device))
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if t.numel() < numel:
+        raise ValueError("%s has %d elements; the call reads %d" % (name, t.numel(), numel))
+    return t
+
+
+def _rows_arg(t: Optional[torch.Tensor], name: str, dtype: torch.dtype, rows: int, cols: int,
+              device) -> Optional[torch.Tensor]:
+    """A 2-D array argument [>= rows, >= cols] whose rows are dense (any row stride)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError("%s must be a 2-D torch tensor" % name)
+    if t.device != device:
+        raise ValueError("%s is on %s; the call runs on %s (the logits' device)" % (name, t.device, device))
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.shape[0] < rows or t.shape[1] < cols:
+        raise ValueError("%s is %s; the call reads [%d, %d]" % (name, tuple(t.shape), rows, cols))
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("%s rows must be dense (stride 1 along a row)" % name)
+    return t
+
+
+def _check_out(out: "VerifyOutputs", batch: int, max_len: int, rows: int, device):
+    i32, i64 = torch.int32, torch.int64
+    _arg(out.accept_len, "out.accept_len", i32, batch, device)
+    _arg(out.num_out, "out.num_out", i32, batch, device)
+    _arg(out.out_tokens, "out.out_tokens", i32, batch * max_len, device)
+    _arg(out.bonus, "out.bonus", i32, batch, device)
+    _arg(out.accept_rows, "out.accept_rows", i32, batch * max_len, device)
+    _arg(out.commit_cu, "out.commit_cu", i32, batch + 1, device)
+    _arg(out.commit_src_slot, "out.commit_src_slot", i64, rows, device)
+    _arg(out.commit_dst_pos, "out.commit_dst_pos", i64, rows, device)
+    _arg(out.dev_status, "out.dev_status", i32, batch, device)
+
+
+def _check_ws(ws: torch.Tensor, device):
+    _arg(ws, "ws", torch.uint8, 0, device)
+
+
 def _stream(stream) -> ctypes.c_void_p:
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
@@ -177,14 +248,25 @@ def _prep(out, ws, batch, max_len, rows, vocab, device, slots):
         out = VerifyOutputs.allocate(batch, max_len, rows, device, slots)
     if ws is None:
         ws = workspace(rows, batch, vocab, max_len, device)
+    _check_out(out, batch, max_len, rows, device)
+    _check_ws(ws, device)
     return out, ws
+
+
+def _chain_args(device, rows, batch, verify_ids, row_slots, seq_lens):
+    _arg(verify_ids, "verify_ids", torch.int32, rows, device)
+    _arg(row_slots, "row_slots", torch.int64, rows, device)
+    _arg(seq_lens, "seq_lens", torch.int64, batch, device)
 
 
 def greedy_chain(logits, verify_ids, m, *, row_slots=None, seq_lens=None, out=None, ws=None, stream=None):
     """Greedy chain verification of logits [batch*(m+1), V]."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch = rows // (m + 1)
+    dev = logits.device
+    _chain_args(dev, batch * (m + 1), batch, verify_ids, row_slots, seq_lens)
     out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_greedy_chain", lib.spec_verify_greedy_chain(
@@ -197,8 +279,15 @@ def rejection_chain(logits, verify_ids, m, q, temperature, u_accept, u_final, *,
                     out=None, ws=None, stream=None):
     """p/q rejection chain verification of logits [batch*(m+1), V] with proposal rows q."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch = rows // (m + 1)
+    dev, R = logits.device, batch * (m + 1)
+    _chain_args(dev, R, batch, verify_ids, row_slots, seq_lens)
+    _rows_arg(q, "q", torch.float32, R, V, dev)
+    _arg(temperature, "temperature", torch.float32, batch, dev)
+    _arg(u_accept, "u_accept", torch.float32, R, dev)
+    _arg(u_final, "u_final", torch.float32, batch, dev)
     out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_rejection_chain", lib.spec_verify_rejection_chain(
@@ -212,8 +301,13 @@ def sample_match_chain(logits, verify_ids, m, temperature, u_sample, *, row_slot
                        ws=None, stream=None):
     """Verification by independent target sampling (u_sample per row) and prefix match."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch = rows // (m + 1)
+    dev, R = logits.device, batch * (m + 1)
+    _chain_args(dev, R, batch, verify_ids, row_slots, seq_lens)
+    _arg(temperature, "temperature", torch.float32, batch, dev)
+    _arg(u_sample, "u_sample", torch.float32, R, dev)
     out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_sample_match_chain", lib.spec_verify_sample_match_chain(
@@ -232,9 +326,19 @@ def rejection_chain_sparse(logits, verify_ids, m, cand_ids, cand_probs, temperat
                            row_slots=None, seq_lens=None, out=None, ws=None, stream=None):
     """p/q rejection chain whose q is given by candidate lists cand_ids / cand_probs [rows, K]."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch = rows // (m + 1)
+    dev, R = logits.device, batch * (m + 1)
+    _chain_args(dev, R, batch, verify_ids, row_slots, seq_lens)
+    _rows_arg(cand_ids, "cand_ids", torch.int32, R, 0, dev)
     K = cand_ids.shape[1]
+    _rows_arg(cand_probs, "cand_probs", torch.float32, R, K, dev)
+    if cand_probs is not None and (cand_probs.shape[1] != K or (K > 1 and cand_probs.stride(0) != cand_ids.stride(0))):
+        raise ValueError("cand_probs must have cand_ids' shape and row stride")
+    _arg(temperature, "temperature", torch.float32, batch, dev)
+    _arg(u_accept, "u_accept", torch.float32, R, dev)
+    _arg(u_final, "u_final", torch.float32, batch, dev)
     if ws is None:
         ws = sparse_workspace(rows, batch, V, m + 1, K, logits.device)
     out, ws = _prep(out, ws, batch, m + 1, rows, V, logits.device, row_slots is not None)
@@ -250,8 +354,16 @@ def rejection_ragged(logits, cu_seqlens, max_len, verify_ids, q, temperature, u_
                      seq_lens=None, out=None, ws=None, stream=None):
     """Ragged p/q rejection verification; cu_seqlens [B+1] int32 (lengths include the anchor)."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
+    dev = logits.device
+    _arg(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
     batch = cu_seqlens.numel() - 1
+    _chain_args(dev, rows, batch, verify_ids, row_slots, seq_lens)
+    _rows_arg(q, "q", torch.float32, rows, V, dev)
+    _arg(temperature, "temperature", torch.float32, batch, dev)
+    _arg(u_accept, "u_accept", torch.float32, rows, dev)
+    _arg(u_final, "u_final", torch.float32, batch, dev)
     out, ws = _prep(out, ws, batch, max_len, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_rejection_ragged", lib.spec_verify_rejection_ragged(
@@ -261,12 +373,24 @@ def rejection_ragged(logits, cu_seqlens, max_len, verify_ids, q, temperature, u_
     return out
 
 
+def _tree_args(device, batch, nodes, tokens, parents, first_child, next_sibling, row_slots, seq_lens):
+    n = batch * nodes
+    _arg(tokens, "tokens", torch.int32, n, device)
+    _arg(parents, "parents", torch.int32, n, device)
+    _arg(first_child, "first_child", torch.int32, n, device)
+    _arg(next_sibling, "next_sibling", torch.int32, n, device)
+    _arg(row_slots, "row_slots", torch.int64, n, device)
+    _arg(seq_lens, "seq_lens", torch.int64, batch, device)
+
+
 def greedy_tree(logits, tokens, parents, *, first_child=None, next_sibling=None, row_slots=None, seq_lens=None,
                 out=None, ws=None, stream=None):
     """Greedy tree verification; tokens / parents [batch, nodes], logits [batch*nodes, V]."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch, nodes = tokens.shape
+    _tree_args(logits.device, batch, nodes, tokens, parents, first_child, next_sibling, row_slots, seq_lens)
     out, ws = _prep(out, ws, batch, nodes, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_greedy_tree", lib.spec_verify_greedy_tree(
@@ -281,8 +405,14 @@ def target_only_tree(logits, tokens, parents, temperature, u_accept, u_final, *,
                      ws=None, stream=None):
     """Target-only tree sampling; u_accept [batch*nodes], u_final [batch]."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     batch, nodes = tokens.shape
+    dev = logits.device
+    _tree_args(dev, batch, nodes, tokens, parents, first_child, next_sibling, row_slots, seq_lens)
+    _arg(temperature, "temperature", torch.float32, batch, dev)
+    _arg(u_accept, "u_accept", torch.float32, batch * nodes, dev)
+    _arg(u_final, "u_final", torch.float32, batch, dev)
     out, ws = _prep(out, ws, batch, nodes, rows, V, logits.device, row_slots is not None)
     st = out.struct()
     _check("spec_verify_target_only_tree", lib.spec_verify_target_only_tree(
@@ -296,8 +426,11 @@ def target_only_tree(logits, tokens, parents, temperature, u_accept, u_final, *,
 def row_stats(logits, row_temp=None, probe=None, ws=None, stream=None) -> dict:
     """Row maximum, lowest argmax, Z (fp64), p at probe and flags for every row."""
     lib = load_library()
+    _require_cuda(logits)
     rows, V = logits.shape
     d = logits.device
+    _arg(row_temp, "row_temp", torch.float32, rows, d)
+    _arg(probe, "probe", torch.int32, rows, d)
     res = {"max": torch.empty(rows, dtype=torch.float32, device=d),
            "argmax": torch.empty(rows, dtype=torch.int32, device=d),
            "z": torch.empty(rows, dtype=torch.float64, device=d),
@@ -305,6 +438,7 @@ def row_stats(logits, row_temp=None, probe=None, ws=None, stream=None) -> dict:
            "flags": torch.empty(rows, dtype=torch.int32, device=d)}
     if ws is None:
         ws = workspace(rows, 1, V, 1, d)
+    _check_ws(ws, d)
     _check("spec_verify_row_stats", lib.spec_verify_row_stats(
         _ptr(logits), _dtype(logits), logits.stride(0), rows, V, _ptr(row_temp), _ptr(probe), _ptr(res["max"]),
         _ptr(res["argmax"]), _ptr(res["z"]), _ptr(res["p"]), _ptr(res["flags"]), _ptr(ws), ws.numel(),
@@ -334,13 +468,18 @@ def dspark_verify_lens(survival, budget: int, *, min_len: int = 1, max_len: Opti
                        out=None, ws=None, stream=None) -> torch.Tensor:
     """verify_lens [R] (int32, on survival's device) from the current survival [R, D]."""
     lib = load_library()
+    _require_cuda(survival, "survival")
     R, D = survival.shape
+    dev = survival.device
+    _rows_arg(survival, "survival", torch.float32, R, D, dev)
     if max_len is None:
         max_len = D + 1
     if out is None:
         out = torch.empty(R, dtype=torch.int32, device=survival.device)
     if ws is None:
         ws = dspark_workspace(R, survival.device)
+    _arg(out, "out", torch.int32, R, dev)
+    _check_ws(ws, dev)
     _check("spec_verify_dspark_verify_lens", lib.spec_verify_dspark_verify_lens(
         _ptr(survival), R, D, survival.stride(0), int(budget), int(min_len), int(max_len), float(eps), _ptr(out),
         _ptr(ws), ws.numel(), _stream(stream)))
@@ -350,8 +489,11 @@ def dspark_verify_lens(survival, budget: int, *, min_len: int = 1, max_len: Opti
 def build_tree(parents, seq_lens=None, stream=None) -> dict:
     """Positions, ancestor mask, retrieve index and child / sibling links from parents [B, N] (int32, device)."""
     lib = load_library()
+    _require_cuda(parents, "parents")
     B, N = parents.shape
     d = parents.device
+    _arg(parents, "parents", torch.int32, B * N, d)
+    _arg(seq_lens, "seq_lens", torch.int64, B, d)
     res = {"positions": torch.empty(B, N, dtype=torch.int64, device=d),
            "mask": torch.empty(B, N, N, dtype=torch.uint8, device=d),
            "retrieve_index": torch.empty(B, N, dtype=torch.int32, device=d),
