@@ -109,3 +109,45 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(specverify, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError):
         specverify.load_library()
+
+
+def test_host_validation_of_the_later_entry_points(lib):
+    """Sparse q, sample-then-match and the tree build refuse bad arguments before touching a GPU."""
+    P = ctypes.c_void_p
+    fake, ws, null = P(0x100000), P(0x200000), None
+    out = _out_struct()
+    out.commit_src_slot = None
+    out.commit_dst_pos = None
+    o = ctypes.byref(out)
+
+    def sparse(batch=2, m=3, cand_ids=fake, cand_probs=fake, k=4, ldc=4, dtype=1):
+        return lib.spec_verify_rejection_chain_sparse(fake, dtype, 64, batch, m, 64, fake, cand_ids, cand_probs, k,
+                                                      ldc, fake, fake, fake, null, null, o, ws, 1 << 30, null)
+
+    assert sparse(cand_ids=null) == 1
+    assert sparse(cand_probs=null) == 1
+    assert sparse(k=0) == 2
+    assert sparse(k=1025, ldc=2048) == 2      # more candidates per row than the sampler holds
+    assert sparse(k=8, ldc=4) == 2            # row stride shorter than the list
+    assert sparse(batch=65536) == 2
+    assert sparse(m=-1) == 2
+    assert sparse(dtype=5) == 3
+
+    def match(batch=2, m=3, u=fake, dtype=1, ld=64):
+        return lib.spec_verify_sample_match_chain(fake, dtype, ld, batch, m, 64, fake, fake, u, null, null, o, ws,
+                                                  1 << 30, null)
+
+    assert match(u=null) == 1
+    assert match(batch=65536) == 2
+    assert match(m=-1) == 2
+    assert match(dtype=9) == 3
+    assert match(ld=68) == 4                  # bf16 rows of 136 bytes: not a multiple of 16
+
+    def tree(batch=2, nodes=8, parents=fake):
+        return lib.spec_verify_build_tree(parents, null, batch, nodes, fake, fake, fake, fake, fake, fake, null)
+
+    assert tree(parents=null) == 1
+    assert tree(nodes=0) == 2
+    assert tree(nodes=1025) == 2              # above the per-request node bound
+    assert tree(batch=-1) == 2
+    assert tree(batch=0) == 0                 # nothing to do, nothing enqueued
