@@ -244,6 +244,40 @@ def test_workspace_reuse_gives_identical_results():
     assert int(ws[: n].sum().item()) != 0  # scratch is in use, counters were reset by the kernels
 
 
+@pytest.mark.parametrize("idx", [4, 5])
+def test_graph_replay_equals_eager(idx):
+    """The benchmark replays the step from a CUDA graph: replayed outputs equal the eager call's bit for bit."""
+    w = wl.config(idx)
+    d = dw.DeviceInputs.from_workload(w)
+    eager = dw.run(w, d, out=dw.outputs_for(w), ws=dw.workspace_for(w))
+    torch.cuda.synchronize()
+    want = eager.to_numpy()
+    out, ws = dw.outputs_for(w), dw.workspace_for(w)
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        dw.run(w, d, out=out, ws=ws)  # per-device caches filled outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        dw.run(w, d, out=out, ws=ws)
+    torch.cuda.synchronize()
+    for k in out.__dict__:
+        t = getattr(out, k)
+        if t is not None:
+            t.fill_(-7)  # the replays must rewrite every output
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    got = out.to_numpy()
+    n = int(want["commit_cu"][-1])  # the KV-commit lists are written up to the committed count only
+    for k in want:
+        if k in ("commit_src_slot", "commit_dst_pos"):
+            assert np.array_equal(want[k][:n], got[k][:n]), k
+        else:
+            assert np.array_equal(want[k], got[k]), k
+
+
 def test_report_flagged_counts():
     """Reports how many requests fell within 1e-6 of a decision threshold."""
     tot = sum(r["requests"] for _, r in REPORT)
