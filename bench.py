@@ -476,6 +476,7 @@ def run_ours(args):
                      "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
         "clocks": clk, "gpu_launches": KERNELS_PER_STEP[w.kind] * launched,
         "e2e": e2e, "cpu_baseline": cpu,
+        "inputs_sha256": w.sha256(),  # first 16 hex digits per input array (rank 0's batch)
     }
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
@@ -518,6 +519,7 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic", "config": dict(describe(w, flush_wanted(args, w)), parallelism="host cores"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "inputs_sha256": w.sha256(),
     }
     print(json.dumps(line), flush=True)
 
