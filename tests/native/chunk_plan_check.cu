@@ -1,4 +1,9 @@
-// Host-side check of the row-statistics chunk plan (no GPU needed).
+// Host-side checks of the workspace layout and of the row-statistics chunk
+// plan (no GPU needed).
+//
+// Layout: every region starts on a 256-byte boundary, in order, and holds what
+// its users index for the given rows, batch, vocabulary, row bound and
+// candidate count.
 //
 // For many shapes and grids: the queue items of every row, found the way the
 // merge kernel finds them, map back to that row, cover its full vectors
@@ -13,8 +18,50 @@
 
 using namespace sv;
 
-int main() {
+// Workspace layout: regions in order, 256-byte aligned, each as large as its users index.
+static int check_ws_layout() {
   int bad = 0, cases = 0;
+  const int64_t rowss[] = {0, 1, 5, 272, 1024, 1152, 65536};
+  const int32_t batches[] = {0, 1, 8, 64, 256, 4096};
+  const int32_t vocabs[] = {1, 3, 1000, 32000, 151936, 262144};
+  const int32_t maxlens[] = {1, 5, 16, 1024};
+  const int32_t cands[] = {0, 1, 16, 1024};
+  for (int64_t R : rowss)
+    for (int32_t B : batches)
+      for (int32_t V : vocabs)
+        for (int32_t ML : maxlens)
+          for (int32_t K : cands) {
+            const WsLayout L = ws_layout(R, B, V, ML, K);
+            ++cases;
+            const size_t r1 = R > 0 ? R : 1, b1 = B > 0 ? B : 1, m1 = ML > 0 ? ML : 1;
+            const size_t nfull = (V > 0 ? V : 1) / 4;
+            const size_t cpr = nfull >= 1 ? (nfull + 1023) / 1024 : 1;  // chunks per row, 1024-vector chunks
+            const size_t starts[] = {L.done_cnt, L.counters_end, L.rowstat, L.partial, L.psb, L.state, L.excl,
+                                     L.ureq, L.cand, L.tsum, L.total};
+            bool ok = L.done_cnt == 0 && L.counters_end >= 16 && L.rowstat >= L.counters_end;
+            for (size_t i = 1; i < sizeof(starts) / sizeof(starts[0]); ++i)
+              ok = ok && starts[i] % 256 == 0 && starts[i] >= starts[i - 1];
+            ok = ok && L.partial - L.rowstat >= sizeof(RowStat) * r1;
+            ok = ok && L.psb - L.partial >= sizeof(RowPartial) * r1 * cpr;
+            ok = ok && L.state - L.psb >= sizeof(float) * r1 * cpr;
+            ok = ok && L.excl - L.state >= sizeof(ReqState) * b1;
+            ok = ok && L.ureq - L.excl >= sizeof(int32_t) * b1 * m1;
+            ok = ok && L.cand - L.ureq >= sizeof(float) * b1;
+            ok = ok && L.cand_cap >= (K > 0 ? K : 1) && L.tsum - L.cand >= 8 * b1 * static_cast<size_t>(L.cand_cap);
+            ok = ok && L.ntiles == (V + kTile - 1) / kTile &&
+                 L.total - L.tsum >= sizeof(uint64_t) * b1 * static_cast<size_t>(L.ntiles > 0 ? L.ntiles : 1);
+            if (!ok) {
+              if (bad < 10)
+                std::printf("ws layout: R=%lld B=%d V=%d ML=%d K=%d\n", (long long)R, B, V, ML, K);
+              ++bad;
+            }
+          }
+  std::printf("workspace layout: %d cases, %d failures\n", cases, bad);
+  return bad;
+}
+
+int main() {
+  int bad = check_ws_layout(), cases = 0;
   const int vocabs[] = {1, 3, 7, 8, 9, 16, 255, 1000, 2048, 4099, 8191, 8192, 8200, 32000, 128256, 151936, 262144};
   const int64_t rowss[] = {1, 2, 5, 17, 64, 272, 1024, 1152, 5000};
   const int grids[] = {1, 3, 40, 152, 456};
@@ -76,6 +123,6 @@ int main() {
               break;
             }
         }
-  std::printf("chunk plan: %d cases, %d failures\n", cases, bad);
+  std::printf("chunk plan: %d cases, %d failures (with the layout's)\n", cases, bad);
   return bad != 0;
 }

@@ -1,9 +1,11 @@
-"""The row-statistics chunk plan, checked on the host (no GPU).
+"""The workspace layout and the row-statistics chunk plan, checked on the host (no GPU).
 
 Compiles tests/native/chunk_plan_check.cu (which includes the statistics
 translation unit) against the library's other objects with nvcc and runs it:
-every row's chunks, found as the merge kernel finds them, must cover the row's
-stages once and in order, and the plan must fit the workspace's partial area.
+the workspace regions must be aligned, ordered and large enough for every
+shape tried; every row's chunks, found as the merge kernel finds them, must
+cover the row's stages once and in order, and the plan must fit the
+workspace's partial area.
 """
 import os
 import shutil
@@ -28,4 +30,4 @@ def test_chunk_plan_covers_every_row_once(tmp_path):
     assert r.returncode == 0, r.stderr[-3000:]
     r = subprocess.run([exe], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout[-3000:]
-    assert "0 failures" in r.stdout
+    assert "layout: " in r.stdout and r.stdout.count(" 0 failures") == 2, r.stdout
