@@ -52,6 +52,9 @@ def parse_args(argv=None):
                     help="rejection-chain workloads verified by independent target sampling and prefix match")
     ap.add_argument("--q-cands", type=int, default=0,
                     help="rejection chains only: q given as K candidates per row (sparse) instead of dense rows")
+    ap.add_argument("--kernel", default="step", choices=["step", "dspark", "tree-build"],
+                    help="step: the verify step (default); dspark: the verify-length scheduler (256 requests x 15 "
+                         "drafts); tree-build: tree-verify inputs from parent arrays (64 trees x 64 nodes)")
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="write a buffer larger than L2 before every step (auto: when the logits are smaller "
                          "than twice the L2); the step time then excludes the flushes")
@@ -550,9 +553,178 @@ def subset(w, n: int):
     return s
 
 
+# ---------------------------------------------------------------------------
+# Scheduler and tree-input builder (their own small kernels, timed the same way)
+# ---------------------------------------------------------------------------
+
+# One lane compares two 64-bit keys in three 32-bit integer instructions (two compares with carry, one
+# predicated add): 152 SMs x 128 lanes x 2.07 GHz / 3.
+ALU_COMPARE_PEAK = 152 * 128 * 2.07e9 / 3.0
+AUX = {"dspark": {"metric": "verify-length schedules/s", "unit": "schedules/s", "launches": 2},
+       "tree-build": {"metric": "tree batches built/s", "unit": "batches/s", "launches": 1}}
+
+
+def aux_inputs(kind: str, rank: int = 0) -> dict:
+    from reject_row_vocab_gb300 import workload as wl
+    if kind == "dspark":
+        return wl.dspark_schedule(requests=256, drafts=15, seed=1006 + 100 * rank)
+    return wl.random_trees(batch=64, nodes=64, fan=8, seed=1007 + 100 * rank)
+
+
+def aux_config(kind: str, x: dict) -> dict:
+    if kind == "dspark":
+        R, D = x["survival"].shape
+        return {"workload": "dspark_schedule_r%d_d%d" % (R, D), "requests": R, "drafts": D,
+                "l2": "inputs of %d KB, L2-resident (a scheduling step, not a streaming pass)" % (R * D * 4 // 1024)}
+    B, N = x["parents"].shape
+    return {"workload": "tree_build_b%d_n%d" % (B, N), "batch": B, "nodes": N,
+            "l2": "inputs and outputs of %d KB, L2-resident" % ((B * N * (N + 28) + 8 * B) // 1024)}
+
+
+def run_aux(args):
+    import numpy as np
+    import torch
+    ranks = Ranks()
+    torch.cuda.set_device(ranks.local)
+    from reject_row_vocab_gb300 import _build
+    if ranks.local == 0:
+        _build.build()
+    ranks.barrier()
+    from reject_row_vocab_gb300 import specverify as sv
+    kind, spec = args.kernel, AUX[args.kernel]
+    x = aux_inputs(kind, ranks.rank)
+    dev = torch.device("cuda", ranks.local)
+    if kind == "dspark":
+        R, D = x["survival"].shape
+        k_star = sv.dspark_budget(x["hist"], R, x["sps"])
+        surv = torch.from_numpy(x["survival"]).to(dev)
+        out = torch.empty(R, dtype=torch.int32, device=dev)
+        ws = sv.dspark_workspace(R, dev)
+
+        def call():
+            sv.dspark_verify_lens(surv, k_star, out=out, ws=ws)
+        work = float(R * D) ** 2  # pairwise key comparisons per call
+    else:
+        B, N = x["parents"].shape
+        par = torch.from_numpy(x["parents"]).to(dev)
+        sl = torch.from_numpy(x["seq_lens"]).to(dev)
+        res = sv.build_tree(par, sl)
+
+        def call():
+            sv.build_tree(par, sl, out=res)
+        # bytes per call: parents and seq_lens read; mask, positions, index, links and status written
+        work = float(B * N * 4 + B * 8 + B * N * N + B * N * (8 + 4 + 4 + 4) + B * 4)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    for _ in range(max(W, 3)):
+        call()
+    torch.cuda.synchronize()
+    G = max(1, min(args.graph_steps, K))
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(G):
+            call()
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for(ranks.local))
+    clocks.start()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    reps = max(1, K // G)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clocks.mark(t0, time.time())
+    clk = clocks.stop()
+    launched = reps * G
+    el = ranks.max(e0.elapsed_time(e1) / 1e3)
+    per_call = el / launched
+    if kind == "dspark":
+        roof = {"bound": "alu", "achieved": work / per_call / 1e9, "peak": ALU_COMPARE_PEAK / 1e9,
+                "unit": "Gcompare/s", "frac": work / per_call / ALU_COMPARE_PEAK, "traffic": None,
+                "kernel": "k_dspark_rank + k_dspark_lens", "compares_per_launch": work,
+                "timed_span": "whole calls inside a CUDA graph", "peak_source": "derived (lanes x clock / 3)"}
+    else:
+        peak, src = measured_peaks()
+        roof = {"bound": "hbm", "achieved": work / per_call / 1e9, "peak": peak, "unit": "GB/s",
+                "frac": work / per_call / 1e9 / peak, "traffic": None, "kernel": "k_build_tree",
+                "bytes_per_launch": work, "timed_span": "whole calls inside a CUDA graph", "peak_source": src}
+    line = {
+        "metric": spec["metric"], "value": ranks.sum(launched) / el, "unit": spec["unit"], "n_gpus": ranks.world,
+        "steps": launched, "warmup": max(W, 3), "ms_per_step": 1e3 * per_call, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if kind == "dspark" else "int32",
+        "data": "synthetic", "config": dict(aux_config(kind, x), launch="cuda graph of %d calls" % G,
+                                            parallelism="replicas x%d (independent inputs)" % ranks.world),
+        "roofline": roof, "clocks": clk, "gpu_launches": spec["launches"] * launched, "e2e": None,
+        "cpu_baseline": None,
+    }
+    if kind == "dspark":
+        line["budget"] = k_star
+        line["verify_lens_sum"] = int(out.sum().item())
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+    ranks.close()
+
+
+def run_aux_reference(args):
+    """The scheduler or the tree builder of the fp64 oracle, on the host, same inputs and config."""
+    import oracle.dspark as od
+    import oracle.tree_build as ot
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    kind, spec = args.kernel, AUX[args.kernel]
+    x = aux_inputs(kind)
+    if kind == "dspark":
+        surv = x["survival"].astype("float64").tolist()
+        R = len(surv)
+        k_star = od.budget(x["hist"].astype("float64").tolist(), R, x["sps"].astype("float64").tolist())
+
+        def call():
+            od.verify_lens(surv, k_star)
+    else:
+        par, sl = x["parents"].tolist(), x["seq_lens"].tolist()
+
+        def call():
+            for b in range(len(par)):
+                ot.build(par[b], sl[b], b)
+    for _ in range(args.warmup if args.warmup < 3 else 3):
+        call()
+    budget = args.ref_budget_s
+    t0 = time.perf_counter()
+    n = 0
+    while n < args.steps and time.perf_counter() - t0 < budget:
+        call()
+        n += 1
+    el = time.perf_counter() - t0
+    value = n / el
+    sample = "%d calls on one host thread (the oracle is single-threaded here)" % n
+    line = {
+        "impl": "reference", "metric": spec["metric"], "value": value, "unit": spec["unit"], "n_gpus": 1,
+        "steps": n, "warmup": min(args.warmup, 3), "ms_per_step": 1e3 * el / n, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(aux_config(kind, x), parallelism="host cores"),
+        "cpu_baseline": {"value": value, "unit": spec["unit"], "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": spec["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
-    if args.impl == "reference":
+    if args.kernel != "step":
+        run_aux_reference(args) if args.impl == "reference" else run_aux(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -486,20 +486,29 @@ def dspark_verify_lens(survival, budget: int, *, min_len: int = 1, max_len: Opti
     return out
 
 
-def build_tree(parents, seq_lens=None, stream=None) -> dict:
-    """Positions, ancestor mask, retrieve index and child / sibling links from parents [B, N] (int32, device)."""
+def build_tree(parents, seq_lens=None, stream=None, out: Optional[dict] = None) -> dict:
+    """Positions, ancestor mask, retrieve index and child / sibling links from parents [B, N] (int32, device).
+
+    out: optional preallocated results with the keys and shapes this function returns."""
     lib = load_library()
     _require_cuda(parents, "parents")
     B, N = parents.shape
     d = parents.device
     _arg(parents, "parents", torch.int32, B * N, d)
     _arg(seq_lens, "seq_lens", torch.int64, B, d)
-    res = {"positions": torch.empty(B, N, dtype=torch.int64, device=d),
-           "mask": torch.empty(B, N, N, dtype=torch.uint8, device=d),
-           "retrieve_index": torch.empty(B, N, dtype=torch.int32, device=d),
-           "first_child": torch.empty(B, N, dtype=torch.int32, device=d),
-           "next_sibling": torch.empty(B, N, dtype=torch.int32, device=d),
-           "status": torch.empty(B, dtype=torch.int32, device=d)}
+    res = out if out is not None else {
+        "positions": torch.empty(B, N, dtype=torch.int64, device=d),
+        "mask": torch.empty(B, N, N, dtype=torch.uint8, device=d),
+        "retrieve_index": torch.empty(B, N, dtype=torch.int32, device=d),
+        "first_child": torch.empty(B, N, dtype=torch.int32, device=d),
+        "next_sibling": torch.empty(B, N, dtype=torch.int32, device=d),
+        "status": torch.empty(B, dtype=torch.int32, device=d)}
+    for k, dt, n in (("positions", torch.int64, B * N), ("mask", torch.uint8, B * N * N),
+                     ("retrieve_index", torch.int32, B * N), ("first_child", torch.int32, B * N),
+                     ("next_sibling", torch.int32, B * N), ("status", torch.int32, B)):
+        if res.get(k) is None:
+            raise ValueError("build_tree: out lacks %r" % k)
+        _arg(res[k], "out[%r]" % k, dt, n, d)
     _check("spec_verify_build_tree", lib.spec_verify_build_tree(
         _ptr(parents), _ptr(seq_lens), B, N, _ptr(res["positions"]), _ptr(res["mask"]), _ptr(res["retrieve_index"]),
         _ptr(res["first_child"]), _ptr(res["next_sibling"]), _ptr(res["status"]), _stream(stream)))

@@ -451,3 +451,33 @@ def config(index: int, **overrides) -> Workload:
         kw.update(overrides)
         return ragged_block(**kw)
     raise ValueError(index)
+
+
+# ----------------------------------------------------------------------------
+# Inputs of the verify-length scheduler and of the tree-input builder
+# ----------------------------------------------------------------------------
+
+
+def dspark_schedule(requests: int = 256, drafts: int = 15, seed: int = 1006) -> dict:
+    """Survival scores of a DSpark-style block ([E2D] §5.6.3–5.6.4): per request, the running product of
+    per-position confidences drawn U(0.5, 1); the previous round's survivals stand in for the history; the speed
+    table (rounds/s by target rows M) falls as 1 / (1 + M / 500)."""
+    rng = np.random.default_rng(seed)
+    conf = rng.uniform(0.5, 1.0, size=(requests, drafts)).astype(np.float32)
+    survival = np.cumprod(conf, axis=1, dtype=np.float32)
+    hist = np.cumprod(rng.uniform(0.5, 1.0, size=(requests, drafts)).astype(np.float32), axis=1,
+                      dtype=np.float32).ravel()
+    sps = (1.0 / (1.0 + np.arange(requests * (drafts + 1) + 1) / 500.0)).astype(np.float32)
+    return {"survival": survival, "hist": hist, "sps": sps}
+
+
+def random_trees(batch: int = 64, nodes: int = 64, fan: int = 8, seed: int = 1007) -> dict:
+    """Parent arrays of draft trees: node i's parent is uniform among the fan nodes before it (chains when
+    fan = 1, bushy trees otherwise), the root first; sequence lengths U{128..4096}."""
+    rng = np.random.default_rng(seed)
+    parents = np.empty((batch, nodes), np.int32)
+    parents[:, 0] = -1
+    for i in range(1, nodes):
+        parents[:, i] = rng.integers(max(0, i - fan), i, size=batch)
+    seq_lens = rng.integers(128, 4097, size=batch).astype(np.int64)
+    return {"parents": parents, "seq_lens": seq_lens}

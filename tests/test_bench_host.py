@@ -37,3 +37,20 @@ def test_traffic_record_applies_only_to_its_workload_and_source():
     assert bench.stats_traffic(_w(base + "_sparse_q16", "rejection_chain_sparse", 1)) == t
     assert bench.stats_traffic(_w(base + "_sample_match", "sample_match_chain", 1)) is None
     assert bench.stats_traffic(_w("c3_greedy_tree", "greedy_tree", 1)) is None
+
+
+def test_aux_modes_inputs_and_reference_arm(capsys):
+    import bench
+    x = bench.aux_inputs("dspark")
+    assert x["survival"].shape == (256, 15) and x["survival"].dtype.name == "float32"
+    assert (x["survival"][:, 1:] <= x["survival"][:, :-1]).all()  # running products only fall
+    t = bench.aux_inputs("tree-build")
+    par = t["parents"]
+    assert par.shape == (64, 64) and (par[:, 0] == -1).all()
+    assert all((par[:, i] >= 0).all() and (par[:, i] < i).all() for i in range(1, 64))
+    assert bench.aux_config("dspark", x)["workload"] == "dspark_schedule_r256_d15"
+    for kind in ("dspark", "tree-build"):
+        bench.main(["--impl", "reference", "--kernel", kind, "--steps", "2", "--warmup", "1"])
+        line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
+        assert line["metric"] == bench.AUX[kind]["metric"]

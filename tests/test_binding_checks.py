@@ -89,13 +89,18 @@ def test_direct_calls_pass_the_checks(cpu_binding):
                     out=sv.VerifyOutputs.allocate(0, 4, 0, "cpu", slots=False))
     surv = torch.rand((40, 8))[:, :6]  # a row-strided view, as the scheduler test passes
     sv.dspark_verify_lens(surv, 50, ws=torch.zeros(64 << 10, dtype=torch.uint8))
-    sv.build_tree(torch.tensor([[-1, 0, 0, 1]], dtype=torch.int32), torch.tensor([7]))
+    par = torch.tensor([[-1, 0, 0, 1]], dtype=torch.int32)
+    res = sv.build_tree(par, torch.tensor([7]))
+    sv.build_tree(par, None, out=res)  # preallocated results pass the same checks
+    bad = dict(res, mask=res["mask"].int())
+    with pytest.raises(TypeError):
+        sv.build_tree(par, None, out=bad)
     with pytest.raises(TypeError):
         sv.build_tree(torch.tensor([[-1, 0, 0, 1]]), None)  # int64 parents
     with pytest.raises(TypeError):
         sv.dspark_verify_lens(surv.double(), 50)
     assert cpu_binding.calls == ["spec_verify_row_stats", "spec_verify_greedy_chain", "spec_verify_dspark_verify_lens",
-                                 "spec_verify_build_tree"]
+                                 "spec_verify_build_tree", "spec_verify_build_tree"]
 
 
 def _chain_case():
