@@ -204,7 +204,8 @@ sv_status_t spec_verify_greedy_chain(const void* logits, sv_dtype_t dtype, int64
   SV_TRY_CUDA(device_info(&dev));
   const LogitsView lg{logits, dtype, ld, rows, vocab};
   SV_TRY_CUDA(row_stats_timed(lg, RowMap{kMapGreedy, m + 1, batch, nullptr, nullptr}, w, stats_grid(dev, lg), stream));
-  ChainParams p{lg, batch, m + 1, m + 1, nullptr, verify_ids, nullptr, 0, nullptr, nullptr, nullptr};
+  ChainParams p{lg,      batch,   m + 1,   m + 1,   nullptr, verify_ids, nullptr, 0,
+                nullptr, nullptr, nullptr, nullptr, nullptr, 0,          0,       0};
   const OutView ov = out_view(out);
   SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
   SV_TRY_CUDA(launch_commit(ov, CommitParams{batch, m + 1, row_slots, seq_lens, w.err}, stream));
@@ -242,7 +243,7 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
     SV_TRY_CUDA(row_stats_timed(lg, map, w, stats_grid(dev, lg), stream));
   }
   ChainParams p{lg,       batch,    max_len,  fixed_len, cu,        verify_ids, q,  ldq,
-                temperature, u_accept, u_final, cand_ids, cand_probs, num_cands, ldc};
+                temperature, u_accept, u_final, cand_ids, cand_probs, num_cands, ldc, 0};
   SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
   SV_TRY_CUDA(launch_sample_and_commit(lg, q, ldq, u_final, ov, CommitParams{batch, max_len, row_slots, seq_lens, w.err},
                                        w, dev, stream, cand_ids != nullptr));
