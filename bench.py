@@ -463,6 +463,8 @@ def run_ours(args):
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds, os.cpu_count() or 1)
+        one = time_oracle(w, args.cpu_seconds / 3.0, 1)  # the same oracle on one host thread
+        cpu["single_thread"] = {"value": one["value"], "cores": 1, "seconds": one["seconds"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": launched,
