@@ -300,6 +300,17 @@ def time_oracle(w, seconds: float, threads: int) -> dict:
                       % (w.batch, w.rows, reps), "seconds": round(el, 3)}
 
 
+def step_parity(w, res: dict, threads: int) -> dict:
+    """The timed step's outputs (the last replay) against the oracle on the same inputs, under the parity rule:
+    exact token decisions except from a decision within 1e-6 of its threshold on."""
+    from oracle import parity
+    c = parity.compare(w, res, oracle_run(w, threads), check=False)
+    return {"requests": c["requests"], "exact": c["exact"], "flagged": c["flagged"],
+            "draw_flagged": c["draw_flagged"], "test_flagged": c["test_flagged"], "differ": c["differ"],
+            "mismatch": c["mismatch"], "rule": "bit-exact decisions; a request is compared up to its first "
+                                              "decision within 1e-6 of its threshold, and must be valid after it"}
+
+
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
@@ -460,11 +471,12 @@ def run_ours(args):
         e2e = {"value": ranks.sum(w.rows * args.e2e_steps) / e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * e_s / args.e2e_steps}
 
-    cpu = None
+    cpu = parity = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         cpu = time_oracle(w, args.cpu_seconds, os.cpu_count() or 1)
         one = time_oracle(w, args.cpu_seconds / 3.0, 1)  # the same oracle on one host thread
         cpu["single_thread"] = {"value": one["value"], "cores": 1, "seconds": one["seconds"]}
+        parity = step_parity(w, res, os.cpu_count() or 1)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ranks.world, "steps": launched,
@@ -480,7 +492,7 @@ def run_ours(args):
                      "bytes_per_launch": alg_bytes,
                      "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
         "clocks": clk, "gpu_launches": KERNELS_PER_STEP[w.kind] * launched,
-        "e2e": e2e, "cpu_baseline": cpu,
+        "e2e": e2e, "cpu_baseline": cpu, "parity": parity,
         "inputs_sha256": w.sha256(),  # first 16 hex digits per input array (rank 0's batch)
     }
     if ranks.rank == 0:

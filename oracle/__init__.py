@@ -31,7 +31,7 @@ def build(force: bool = False) -> str:
 class _Out(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "accept_len", "num_out", "out_tokens", "bonus", "accept_rows", "commit_cu",
-        "commit_src_slot", "commit_dst_pos", "status", "min_gap")]
+        "commit_src_slot", "commit_dst_pos", "status", "min_gap", "test_gap", "draw_gap")]
 
 
 def _load():
@@ -79,6 +79,8 @@ def _alloc_out(batch: int, max_len: int, rows: int) -> dict:
         "commit_dst_pos": np.full(max(rows, 1), -1, np.int64),
         "status": np.zeros(batch, np.uint32),
         "min_gap": np.zeros(batch, np.float64),
+        "test_gap": np.zeros((batch, max_len), np.float64),  # per step: gap of the acceptance test(s) made there
+        "draw_gap": np.zeros(batch, np.float64),             # gap of the final draw
     }
 
 

@@ -38,7 +38,8 @@ def verify_chain_match(w) -> dict:
          "accept_rows": np.full((B, ML), -1, np.int32), "commit_cu": np.zeros(B + 1, np.int32),
          "commit_src_slot": np.full(max(w.rows, 1), -1, np.int64),
          "commit_dst_pos": np.full(max(w.rows, 1), -1, np.int64),
-         "status": np.zeros(B, np.uint32), "min_gap": np.full(B, np.inf)}
+         "status": np.zeros(B, np.uint32), "min_gap": np.full(B, np.inf),
+         "test_gap": np.full((B, ML), np.inf), "draw_gap": np.full(B, np.inf)}
     for b in range(B):
         start, L = int(cu[b]), int(cu[b + 1] - cu[b])
         T = float(w.temperature[b]) if w.temperature is not None else 0.0
@@ -51,15 +52,19 @@ def verify_chain_match(w) -> dict:
                 status |= NONFINITE
                 s, tok = j, -1
                 break
+            g = np.inf
             if _sampling(T):
                 p = oracle.row_probs(w.logits, w.dtype, row, T)
                 t, g = oracle.sample_index(p, float(w.u_accept[row]))
                 gap = min(gap, g)
             else:
                 t = int(st_all["argmax"][row])
-            if j == L - 1:
+            if j == L - 1:  # the last row's draw only emits a token
+                o["draw_gap"][b] = g
                 s, tok = j, int(t)
                 break
+            # a tested row's draw decides the match and, at a mismatch, the emitted token
+            o["test_gap"][b, j] = g
             d = int(ids[row + 1])
             if d < 0 or d >= V:
                 status |= TOKEN_RANGE

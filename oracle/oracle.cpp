@@ -43,12 +43,22 @@
 //   * a tree that fails validation is verified as its root alone (status bit 4).
 //   * a request whose row range is invalid commits nothing (status bit 8).
 //
-// min_gap[b] reports, for each request, the smallest distance between a caller
-// uniform and the threshold that decided an acceptance or a sample on that
-// request's path (|u - p/q|, |u - c/theta|, |p - theta_single|, or the distance
-// of u to the two CDF edges of the sampled index).  Decisions with a gap below
-// 1e-6 are the ones a finite-precision implementation may legitimately take
-// the other way.
+// Decision gaps.  For each request the oracle reports how far each decision on
+// its path was from going the other way, in the units of the caller's uniform:
+//   test_gap[b, k]  the acceptance test(s) made at step k of the path (chain row
+//                   start + k, or the tree node at depth k): |u - p/q| for a p/q
+//                   test; min(|u - c/theta_acc|, |p - theta_single|) over the
+//                   children tried for a target-only node; +inf where no test
+//                   was made (greedy steps, steps past the end of the path);
+//   draw_gap[b]     the final inverse-CDF draw: the distance of u to the nearer
+//                   CDF edge of the drawn index that some u in [0, 1) can cross
+//                   (the lower edge when a positive weight lies before the
+//                   index, the upper edge when one lies after it); +inf when
+//                   no draw was made or the weights have a single positive entry;
+//   min_gap[b]      the minimum of the above.
+// A decision whose gap is below 1e-6 is one a finite-precision implementation
+// may legitimately take the other way; every decision before the first such
+// one is certain.
 
 #include <algorithm>
 #include <cmath>
@@ -146,8 +156,12 @@ void residual(const std::vector<double>& p, const float* q, std::vector<double>&
 }
 
 // Inverse CDF over unnormalised weights: the smallest v whose running sum
-// exceeds u * S.  Returns -1 when S <= 0.  *gap: distance of u to the two
-// normalised CDF edges of the chosen index (0 when the fallback fired).
+// exceeds u * S.  Returns -1 when S <= 0.  *gap: distance of u to the nearer
+// normalised CDF edge of the chosen index that a uniform in [0, 1) can cross.
+// The lower edge counts only when positive weight lies before the index (with
+// none, t = u*S >= 0 never falls below it); the upper edge only when positive
+// weight lies after it (with none, it is S itself, and t < S for u < 1).
+// +inf when neither edge counts; 0 when the rounding fallback fired.
 int64_t sample_index(const double* w, int64_t n, double u, double* gap) {
   double S = 0.0;
   for (int64_t v = 0; v < n; ++v) S += w[v];
@@ -161,7 +175,9 @@ int64_t sample_index(const double* w, int64_t n, double u, double* gap) {
     double prev = cum;
     cum += w[v];
     if (cum > t) {
-      *gap = std::min(t - prev, cum - t) / S;
+      const double lower = prev > 0.0 ? (t - prev) / S : kInf;
+      const double upper = cum < S ? (cum - t) / S : kInf;
+      *gap = std::min(lower, upper);
       return v;
     }
   }
@@ -182,6 +198,8 @@ struct Out {
   int64_t* commit_dst_pos;
   uint32_t* status;
   double* min_gap;
+  double* test_gap;  // [B, max_len] or NULL
+  double* draw_gap;  // [B] or NULL
 };
 
 struct ReqResult {
@@ -191,7 +209,19 @@ struct ReqResult {
   std::vector<int32_t> tokens;  // accepted draft tokens
   std::vector<int32_t> rows;    // rows committed: anchor row then accepted rows
   uint32_t status = 0;
-  double gap = kInf;
+  double gap = kInf;                // minimum over every decision below
+  std::vector<double> test_gap;     // per step of the path: the acceptance test(s) made there
+  double draw_gap = kInf;           // the final draw
+
+  void test_at(size_t step, double g) {
+    if (test_gap.size() <= step) test_gap.resize(step + 1, kInf);
+    test_gap[step] = std::min(test_gap[step], g);
+    gap = std::min(gap, g);
+  }
+  void draw(double g) {
+    draw_gap = std::min(draw_gap, g);
+    gap = std::min(gap, g);
+  }
 };
 
 void write_request(const Out& o, int32_t b, int32_t max_len, const ReqResult& rr) {
@@ -200,7 +230,11 @@ void write_request(const Out& o, int32_t b, int32_t max_len, const ReqResult& rr
   o.bonus[b] = rr.bonus;
   o.status[b] = rr.status;
   if (o.min_gap) o.min_gap[b] = rr.gap;
+  if (o.draw_gap) o.draw_gap[b] = rr.draw_gap;
   for (int32_t k = 0; k < max_len; ++k) {
+    if (o.test_gap)
+      o.test_gap[static_cast<int64_t>(b) * max_len + k] =
+          static_cast<size_t>(k) < rr.test_gap.size() ? rr.test_gap[k] : kInf;
     int32_t tok = -1, row = -1;
     if (rr.committed && k < rr.r) tok = rr.tokens[k];
     if (rr.committed && k == rr.r) tok = rr.bonus;
@@ -298,7 +332,7 @@ ReqResult verify_chain_request(const ChainArgs& a, int32_t b) {
       const double qd = static_cast<double>(a.q[row * a.ldq + d]);
       const double u = static_cast<double>(a.u_accept[row]);
       ok = accept_pq(p, qd, u);
-      if (qd > 0.0) rr.gap = std::min(rr.gap, std::fabs(u - p / qd));
+      if (qd > 0.0) rr.test_at(static_cast<size_t>(j), std::fabs(u - p / qd));
     }
     if (!ok) {
       how = kRejected;
@@ -336,7 +370,7 @@ ReqResult verify_chain_request(const ChainArgs& a, int32_t b) {
     rr.status |= kResidualEmpty;
     v = sample_index(p.data(), static_cast<int64_t>(p.size()), a.u_final[b], &gap);
   }
-  rr.gap = std::min(rr.gap, gap);
+  rr.draw(gap);
   rr.bonus = static_cast<int32_t>(v);
   return rr;
 }
@@ -454,7 +488,7 @@ ReqResult verify_tree_request(const TreeArgs& a, int32_t b) {
         seen.push_back(tok[k]);
         const double pk = prob(st, a.lg.at(row, tok[k]));
         c += pk;
-        rr.gap = std::min({rr.gap, std::fabs(u - c / a.th_acc), std::fabs(pk - a.th_single)});
+        rr.test_at(rr.tokens.size(), std::min(std::fabs(u - c / a.th_acc), std::fabs(pk - a.th_single)));
         if (u < c / a.th_acc || pk >= a.th_single) {
           next = k;
           break;
@@ -470,7 +504,7 @@ ReqResult verify_tree_request(const TreeArgs& a, int32_t b) {
           rr.status |= kResidualEmpty;
           v = sample_index(p.data(), static_cast<int64_t>(p.size()), a.u_final[b], &gap);
         }
-        rr.gap = std::min(rr.gap, gap);
+        rr.draw(gap);
         rr.bonus = static_cast<int32_t>(v);
         break;
       }
@@ -502,6 +536,8 @@ typedef struct {
   int64_t* commit_dst_pos;
   uint32_t* status;
   double* min_gap;
+  double* test_gap;  // [B, max_len] per-step acceptance-test gaps, or NULL
+  double* draw_gap;  // [B] final-draw gaps, or NULL
 } oracle_out_t;
 
 // Chain or ragged verification.  greedy_all != 0 verifies every request
@@ -517,7 +553,8 @@ int oracle_verify_chain(int greedy_all, const void* logits, int dtype, int64_t l
   ChainArgs a{{logits, dtype, ld, vocab}, greedy_all != 0, batch, total_rows, max_len, cu_seqlens,
               verify_ids, q, ldq, temperature, u_accept, u_final};
   Out o{out->accept_len, out->num_out, out->out_tokens, out->bonus, out->accept_rows,
-        out->commit_cu, out->commit_src_slot, out->commit_dst_pos, out->status, out->min_gap};
+        out->commit_cu, out->commit_src_slot, out->commit_dst_pos, out->status, out->min_gap,
+        out->test_gap, out->draw_gap};
   for_requests(batch, threads, [&](int32_t b) { write_request(o, b, max_len, verify_chain_request(a, b)); });
   commit(o, batch, max_len, row_slots, seq_lens);
   return 0;
@@ -536,7 +573,8 @@ int oracle_verify_tree(int mode, const void* logits, int dtype, int64_t ld, int3
              (first_child && next_sibling) ? next_sibling : nullptr,
              temperature, threshold_single, threshold_acc, u_accept, u_final};
   Out o{out->accept_len, out->num_out, out->out_tokens, out->bonus, out->accept_rows,
-        out->commit_cu, out->commit_src_slot, out->commit_dst_pos, out->status, out->min_gap};
+        out->commit_cu, out->commit_src_slot, out->commit_dst_pos, out->status, out->min_gap,
+        out->test_gap, out->draw_gap};
   for_requests(batch, threads, [&](int32_t b) { write_request(o, b, nodes, verify_tree_request(a, b)); });
   commit(o, batch, nodes, row_slots, seq_lens);
   return 0;

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 import oracle  # noqa: E402
 from reject_row_vocab_gb300 import _build  # noqa: E402
 from reject_row_vocab_gb300 import workload as wl  # noqa: E402
-from tests.gpu_compare import compare, oracle_outputs  # noqa: E402
+from tests.gpu_compare import compare, flag_bound, oracle_outputs  # noqa: E402
 from tests.helpers import chain_workload, tree_workload  # noqa: E402
 
 if not torch.cuda.is_available():
@@ -24,9 +24,6 @@ if not torch.cuda.is_available():
 _build.build()
 from reject_row_vocab_gb300 import device_workload as dw  # noqa: E402
 from reject_row_vocab_gb300 import specverify as sv  # noqa: E402
-
-REPORT = []
-
 
 def run_gpu(w, use_lists=False, ws=None, out=None):
     d = dw.DeviceInputs.from_workload(w)
@@ -41,7 +38,6 @@ def check(w, use_lists=False):
     g = run_gpu(w, use_lists=use_lists)
     o = oracle_outputs(w, use_lists=use_lists)
     res = compare(w, g, o)
-    REPORT.append((w.name, res))
     return g, o, res
 
 
@@ -137,10 +133,14 @@ def test_chain_and_tree_entry_points_agree():
 def test_full_size_configs(idx, mode):
     w = wl.config(idx, mode=mode) if mode else wl.config(idx)
     g, o, res = check(w)
-    # Flagged requests (a uniform within 1e-6 of a threshold; over a 152k-entry vocabulary
-    # that includes most draws of a rare token) are reported, not compared.
-    print("\n%s: %d requests, %d flagged, %d of those differ" % (w.name, res["requests"], res["flagged"],
-                                                                res["differ_flagged"]))
+    # A request is flagged when a decision's uniform lies within 1e-6 of its threshold; over a
+    # 152k-entry vocabulary about 3 % of draws land on a token whose whole CDF interval is that
+    # narrow.  Flagged requests are still compared up to that decision; the counts are bounded.
+    msg = "%s: %d requests, %d exact, %d draw-flagged, %d test-flagged, %d differ" % (
+        w.name, res["requests"], res["exact"], res["draw_flagged"], res["test_flagged"], res["differ"])
+    assert res["draw_flagged"] <= flag_bound(w.batch, 0.15), msg
+    assert res["test_flagged"] <= flag_bound(w.batch, 0.05), msg
+    assert res["differ"] <= res["flagged"], msg
     # accepted lengths stay within [0, max_len - 1]; tau = E[r + 1] within [1, k + 1]
     assert np.all((g["accept_len"] >= 0) & (g["accept_len"] < w.max_len))
 
@@ -276,11 +276,3 @@ def test_graph_replay_equals_eager(idx):
             assert np.array_equal(want[k][:n], got[k][:n]), k
         else:
             assert np.array_equal(want[k], got[k]), k
-
-
-def test_report_flagged_counts():
-    """Reports how many requests fell within 1e-6 of a decision threshold."""
-    tot = sum(r["requests"] for _, r in REPORT)
-    fl = sum(r["flagged"] for _, r in REPORT)
-    print("\nparity report: %d requests compared, %d flagged near a threshold, %d of those differ"
-          % (tot, fl, sum(r["differ_flagged"] for _, r in REPORT)))
