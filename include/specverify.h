@@ -254,11 +254,13 @@ sv_status_t spec_verify_target_only_tree(const void* logits, sv_dtype_t dtype, i
  * GPU that uses the library keeps it until the process exits) and allocates
  * nothing.  Problems whose workspace would exceed that size
  * (spec_verify_workspace_bytes(batch*(m+1), batch, vocab, m+1) >
- * SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE_TOO_SMALL before anything is
- * enqueued.  The first call on each device looks up the area's device address;
- * make it before any stream capture starts.  Every call clears the area's
- * counters on `stream` before launching; all calls share the area, so calls
- * that overlap on the GPU (other streams or host threads) race — serialise them.
+ * SV_NOALLOC_SCRATCH_BYTES) return SV_ERR_WORKSPACE_TOO_SMALL, and argument
+ * errors their status code, before anything is enqueued or any CUDA call is
+ * made.  The first call in each CUDA context (on each device, and again after a
+ * device reset) looks up the area's device address; make it before any stream
+ * capture starts.  Every call clears the area's counter words on `stream` before
+ * launching; all calls share the area, so calls that overlap on the GPU (other
+ * streams or host threads) race — serialise them.
  */
 #define SV_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
@@ -267,6 +269,27 @@ sv_status_t spec_verify_rejection_chain_noalloc(const void* logits, sv_dtype_t d
                                                 int64_t ldq, const float* temperature, const float* u_accept,
                                                 const float* u_final, const int64_t* row_slots,
                                                 const int64_t* seq_lens, const sv_out_t* out, cudaStream_t stream);
+
+/*
+ * Test and diagnostic hooks (the pages have no counterpart; not for production use).
+ *
+ * spec_verify_noalloc_fill_counters sets every byte of the no-allocation scratch
+ * area's counter words (the words each spec_verify_rejection_chain_noalloc call
+ * clears before it launches) to value & 0xff, on `stream`, in the current
+ * context: a test uses it to show that a call does not depend on what an earlier
+ * call left there.  Returns SV_ERR_CUDA if the area cannot be reached.
+ *
+ * spec_verify_set_hand_off_limit_ns(ns), ns > 0, puts the row-statistics kernel
+ * of every later call, in every thread, into its expiry test: each in-CTA
+ * hand-off wait gives up after ns nanoseconds, and one wait on a barrier that
+ * nothing completes is sure to; the kernel then stops, waits (with the normal
+ * one-second limit) for its own bulk copies still in flight, and raises the
+ * workspace error word, so the call's requests report SV_DEV_TIMEOUT.  ns = 0
+ * (the default) restores normal operation.  After a timed-out call, zero-fill
+ * the workspace before using it again.  Always returns SV_OK.
+ */
+sv_status_t spec_verify_noalloc_fill_counters(uint32_t value, cudaStream_t stream);
+sv_status_t spec_verify_set_hand_off_limit_ns(uint64_t ns);
 
 /*
  * Row statistics on their own (the single pass every entry point starts

@@ -218,7 +218,8 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
                                     const float* temperature, const float* u_accept, const float* u_final,
                                     const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
                                     void* ws, size_t ws_bytes, cudaStream_t stream, const int32_t* cand_ids = nullptr,
-                                    const float* cand_probs = nullptr, int32_t num_cands = 0, int64_t ldc = 0) {
+                                    const float* cand_probs = nullptr, int32_t num_cands = 0, int64_t ldc = 0,
+                                    bool clear_counters = false) {
   if (batch > 65535) return SV_ERR_BAD_SHAPE;  // the sampler's grid has one y-slice per request
   if (batch == 0) return empty_batch(out, stream);
   SV_TRY(check_logits(logits, dtype, ld, rows, vocab));
@@ -235,6 +236,9 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
   SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w, cand_ids ? num_cands : 0));
   DeviceInfo dev{};
   SV_TRY_CUDA(device_info(&dev));
+  if (clear_counters)
+    SV_TRY_CUDA(cudaMemsetAsync(w.done_cnt, 0, ws_layout(rows, batch, vocab, max_len, cand_ids ? num_cands : 0).counters_end,
+                                stream));
   const LogitsView lg{logits, dtype, ld, rows, vocab};
   const OutView ov = out_view(out);
   if (rows > 0) {
@@ -255,11 +259,32 @@ sv_status_t spec_verify_rejection_chain(const void* logits, sv_dtype_t dtype, in
                                         const float* temperature, const float* u_accept, const float* u_final,
                                         const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out,
                                         void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return rejection_chain_entry(logits, dtype, ld, batch, m, vocab, verify_ids, q, ldq, temperature, u_accept,
+                               u_final, row_slots, seq_lens, out, ws, ws_bytes, stream, false);
+}
+
+sv_status_t spec_verify_set_hand_off_limit_ns(uint64_t ns) {
+  set_hand_off_limit_ns(ns);
+  return SV_OK;
+}
+
+}  // extern "C"
+
+namespace sv {
+sv_status_t rejection_chain_entry(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch, int32_t m,
+                                  int32_t vocab, const int32_t* verify_ids, const float* q, int64_t ldq,
+                                  const float* temperature, const float* u_accept, const float* u_final,
+                                  const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream, bool clear_counters) {
   if (batch < 0 || m < 0 || m >= (1 << 20)) return SV_ERR_BAD_SHAPE;
   const int64_t rows = static_cast<int64_t>(batch) * (m + 1);
   return rejection_common(logits, dtype, ld, batch, rows, m + 1, m + 1, vocab, nullptr, verify_ids, q, ldq,
-                          temperature, u_accept, u_final, row_slots, seq_lens, out, ws, ws_bytes, stream);
+                          temperature, u_accept, u_final, row_slots, seq_lens, out, ws, ws_bytes, stream, nullptr,
+                          nullptr, 0, 0, clear_counters);
 }
+}  // namespace sv
+
+extern "C" {
 
 sv_status_t spec_verify_sample_match_chain(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,
                                            int32_t m, int32_t vocab, const int32_t* verify_ids,

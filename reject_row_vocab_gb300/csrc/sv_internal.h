@@ -259,6 +259,18 @@ cudaError_t launch_row_stats(const LogitsView& lg, const RowMap& map, const Ws& 
                              const int32_t* probe = nullptr, int32_t probe_rpr = 0,
                              cudaEvent_t stats_done = nullptr);
 
+// Test hook: the limit (ns) of the statistics kernel's in-CTA hand-off waits, with a forced expiry (see
+// k_row_stats); 0 restores normal operation.  Read at each launch.
+void set_hand_off_limit_ns(uint64_t ns);
+
+// The p/q rejection chain entry point.  clear_counters: after every host check has passed, zero the workspace's
+// counter words on the stream before the first kernel (for a workspace shared between calls).
+sv_status_t rejection_chain_entry(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch, int32_t m,
+                                  int32_t vocab, const int32_t* verify_ids, const float* q, int64_t ldq,
+                                  const float* temperature, const float* u_accept, const float* u_final,
+                                  const int64_t* row_slots, const int64_t* seq_lens, const sv_out_t* out, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream, bool clear_counters);
+
 // Records ev on stream (as an event node while the stream is being captured).
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t stream);
 int stats_grid(const DeviceInfo& dev, const LogitsView& lg);

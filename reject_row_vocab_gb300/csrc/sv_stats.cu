@@ -25,6 +25,7 @@
 // streamed what.  No CTA waits on another.  Every mbarrier wait is bounded (one
 // second); a timeout raises the workspace error word, reported by the next
 // kernels as SV_DEV_TIMEOUT.
+#include <atomic>
 #include <cstdint>
 
 #include "sv_device.cuh"
@@ -115,6 +116,7 @@ struct StatsSmem {
   float tab_ik[kTabCap];   // T/log2(e), the reciprocal of tab_k (0 for greedy rows)
   int32_t tab_cu[kTabCap]; // request offsets of a ragged layout
   unsigned long long tab_ready;
+  unsigned long long never;            // no thread ever arrives: the expiry test waits on it
   unsigned long long full[kStages];    // producer -> consumers (bulk-copy bytes)
   unsigned long long empty[kStages];   // consumers -> producer
   unsigned long long pfull[kSlots];    // consumers -> finalizer
@@ -538,9 +540,15 @@ __device__ __forceinline__ void chunk_merge(Part& a, const Part& b, float k) {
 // PFX: probe-aware pass (each row's probe token probe[row], for every row but
 // the last of each block of probe_rpr rows): the chunk holding the probe also
 // sums the terms of the ids below it.
+// hand_off_ns: 0 in normal use.  Otherwise (a test of the expiry path) every
+// in-CTA hand-off wait (stage full / empty, partial slots) gives up after
+// hand_off_ns, and the finalizer first waits on a barrier that nothing
+// completes, so at least one wait runs out; the waits that drain bulk copies
+// still in flight keep the full limit.
 template <int DT, bool PFX>
 __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, RowMap map, Ws ws, ChunkPlan plan,
-                                                                const int32_t* probe, int32_t probe_rpr) {
+                                                                const int32_t* probe, int32_t probe_rpr,
+                                                                uint64_t hand_off_ns) {
   using VT = VecTraits<DT>;
   constexpr int E = VT::E;
   const int64_t n_items = plan.n_items;
@@ -562,6 +570,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       mbar_init(smem_addr(&sm.pempty[s]), 1);
     }
     mbar_init(smem_addr(&sm.tab_ready), 1);
+    mbar_init(smem_addr(&sm.never), 1);
     sm.abort = 0;
     mbar_fence_init();
   }
@@ -569,6 +578,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
   grid_dependency_wait();  // the logits may come from the previous kernel on the stream
   allow_dependents();
 
+  const uint64_t lim = hand_off_ns ? hand_off_ns : kWaitLimitNs;  // hand-off waits
   const int32_t tab_n = map_table_size(map, lg.rows);
   const bool tabbed = tab_n > 0 && tab_n <= kTabCap;
   if (warp == kProducerWarp) {  // ------------------------------------------ producer
@@ -625,8 +635,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         const int32_t rem = cn - s * kChunkVecs;
         const int32_t n = rem <= 0 ? 0 : (rem < kChunkVecs ? rem : kChunkVecs);
         if (lane == 0) {
-          ok = mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs,
-                                 kProducerNap);
+          ok = mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, lim, kProducerNap);
           if (ok && n > 0) {
             mbar_expect_tx(smem_addr(&sm.full[st]), n * 16);
             bulk_copy_g2s(smem_addr(&sm.buf[st][0]),
@@ -689,7 +698,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         atomicOr(ws.err, 1u);
       } else if (!*abort) {  // end marker
         const int st = g % kStages;
-        if (mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, kWaitLimitNs)) {
+        if (mbar_wait_bounded(smem_addr(&sm.empty[st]), ((g / kStages) & 1u) ^ 1u, &sm.abort, lim)) {
           sm.meta[st] = StageMeta{-1, 0, 0, 0, 0.0f, 0.0f, 0, 0, -1};
           mbar_arrive(smem_addr(&sm.full[st]));
           ended = true;
@@ -741,11 +750,22 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.tab_ready));
     }
+    if (hand_off_ns) {  // expiry test: a wait that nothing completes runs out like a stalled hand-off
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(smem_addr(&sm.never), 0u, &sm.abort, hand_off_ns, kConsumerNap);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) {
+          sm.abort = 1;
+          atomicOr(ws.err, 1u);
+        }
+        return;
+      }
+    }
     // Each chunk's partial goes to the workspace; k_row_merge combines them
     // per row after this grid completes (no cross-CTA waiting here).
     for (uint32_t c = 0;; ++c) {
       const int sl = c % kSlots;
-      if (!mbar_wait_bounded(smem_addr(&sm.pfull[sl]), (c / kSlots) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+      if (!mbar_wait_bounded(smem_addr(&sm.pfull[sl]), (c / kSlots) & 1u, &sm.abort, lim, kConsumerNap)) {
         sm.abort = 1;
         atomicOr(ws.err, 1u);
         break;
@@ -776,8 +796,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
   // Hand a chunk's warp partial (or the end mark, item < 0) to the finalizer.
   auto hand_over = [&](uint32_t c, const Part& p, int32_t item, int32_t row, float k, float sbw) -> bool {
     const int sl = c % kSlots;
-    if (!mbar_wait_bounded(smem_addr(&sm.pempty[sl]), ((c / kSlots) & 1u) ^ 1u, &sm.abort, kWaitLimitNs,
-                           kConsumerNap)) {
+    if (!mbar_wait_bounded(smem_addr(&sm.pempty[sl]), ((c / kSlots) & 1u) ^ 1u, &sm.abort, lim, kConsumerNap)) {
       sm.abort = 1;
       atomicOr(ws.err, 1u);
       return false;
@@ -798,7 +817,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
   uint32_t g = 0;  // stages consumed
   for (uint32_t c = 0;; ++c) {
     int st = g % kStages;
-    if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+    if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, lim, kConsumerNap)) {
       sm.abort = 1;
       atomicOr(ws.err, 1u);
       break;
@@ -832,7 +851,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         ++g;
         if (s + 1 == nst) break;
         st = g % kStages;
-        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, lim, kConsumerNap)) {
           ok = false;
           break;
         }
@@ -859,7 +878,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         ++g;
         if (s + 1 == nst) break;
         st = g % kStages;
-        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, kWaitLimitNs, kConsumerNap)) {
+        if (!mbar_wait_bounded(smem_addr(&sm.full[st]), (g / kStages) & 1u, &sm.abort, lim, kConsumerNap)) {
           ok = false;
           break;
         }
@@ -966,6 +985,12 @@ __global__ void k_export_stats(LogitsView lg, Ws ws, const int32_t* probe, float
 
 }  // namespace
 
+namespace {
+std::atomic<uint64_t> g_hand_off_ns{0};  // 0: hand-off waits use the normal limit
+}  // namespace
+
+void set_hand_off_limit_ns(uint64_t ns) { g_hand_off_ns.store(ns, std::memory_order_relaxed); }
+
 template <int DT>
 cudaError_t stats_occupancy_t(int* blocks_per_sm) {
   cudaError_t e = cudaFuncSetAttribute(k_row_stats<DT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1019,7 +1044,7 @@ cudaError_t launch_row_stats_t(const LogitsView& lg, const RowMap& map, const Ws
                                cudaEvent_t stats_done) {
   const dim3 mgrid(static_cast<unsigned>((lg.rows + 7) / 8));
   cudaError_t e = launch_pdl(k_row_stats<DT, PFX>, dim3(grid), dim3(kStatsThreads), kStatsSmemBytes, stream, lg, map,
-                             ws, plan, probe, probe_rpr);
+                             ws, plan, probe, probe_rpr, g_hand_off_ns.load(std::memory_order_relaxed));
   if (e != cudaSuccess) return e;
   if (stats_done && (e = record_event(stats_done, stream)) != cudaSuccess) return e;
   return launch_pdl(k_row_merge<DT, PFX>, mgrid, dim3(256), 0, stream, lg, ws, plan, probe, probe_rpr);

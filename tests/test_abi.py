@@ -103,6 +103,30 @@ def test_host_validation_without_gpu(lib):
                                             null, ctypes.byref(out2), ws, 1 << 30, null) == 2
 
 
+def test_no_alloc_entry_checks_arguments_before_any_cuda_call(lib):
+    """Refusals of the no-allocation entry come before its scratch lookup and its counter clear: without a GPU
+    they still return the argument's own status, not SV_ERR_CUDA."""
+    P = ctypes.c_void_p
+    fake, null = P(0x100000), None
+    out = _out_struct()
+    out.commit_src_slot = None
+    out.commit_dst_pos = None
+    fn = lib.spec_verify_rejection_chain_noalloc
+    I32, I64 = ctypes.c_int32, ctypes.c_int64
+    fn.argtypes = [P, ctypes.c_int, I64, I32, I32, I32, P, P, I64, P, P, P, P, P, P, P]
+    fn.restype = ctypes.c_int
+
+    def call(verify_ids=fake, q=fake, ldq=64, dtype=1, batch=2, vocab=64):
+        return fn(fake, dtype, 64, batch, 3, vocab, verify_ids, q, ldq, fake, fake, fake, null, null,
+                  ctypes.byref(out), null)
+
+    assert call(verify_ids=null) == 1
+    assert call(q=null) == 1
+    assert call(ldq=65) == 4
+    assert call(dtype=4) == 3
+    assert call(batch=4096, vocab=1 << 20) == 6
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from reject_row_vocab_gb300 import specverify
     monkeypatch.setattr(specverify, "_lib", None)

@@ -27,16 +27,32 @@ def test_flush_choice_follows_l2_size():
     assert "not flushed" in bench.describe(small, False)["l2"]
 
 
-def test_traffic_record_applies_only_to_its_workload_and_source():
+def test_traffic_record_applies_only_to_its_workload_and_source(tmp_path, monkeypatch):
+    """The ncu traffic figure is used only for its own workload and only while the kernel source it was
+    captured from is unchanged (checked on a copy of the tree)."""
+    import hashlib
+    import shutil
+
     import bench
-    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-        rec = json.load(f)
+    for rel in bench.STATS_SOURCES:
+        os.makedirs(os.path.dirname(tmp_path / rel), exist_ok=True)
+        shutil.copy(os.path.join(ROOT, rel), tmp_path / rel)
+    h = hashlib.sha256()
+    for rel in bench.STATS_SOURCES:
+        h.update(open(tmp_path / rel, "rb").read())
+    os.makedirs(tmp_path / "profiles")
+    rec = {"workload_name": "c4_dflash_block", "bytes_per_full_launch": 123.0, "source_sha256": h.hexdigest()}
+    with open(tmp_path / "profiles" / "traffic.json", "w") as f:
+        json.dump(rec, f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     base = rec["workload_name"]
-    t = bench.stats_traffic(_w(base, "rejection_chain", 1))
-    assert t == rec["bytes_per_full_launch"]  # the committed record matches the committed kernel source
-    assert bench.stats_traffic(_w(base + "_sparse_q16", "rejection_chain_sparse", 1)) == t
+    assert bench.stats_traffic(_w(base, "rejection_chain", 1)) == 123.0
+    assert bench.stats_traffic(_w(base + "_sparse_q16", "rejection_chain_sparse", 1)) == 123.0
     assert bench.stats_traffic(_w(base + "_sample_match", "sample_match_chain", 1)) is None
     assert bench.stats_traffic(_w("c3_greedy_tree", "greedy_tree", 1)) is None
+    with open(tmp_path / bench.STATS_SOURCES[0], "a") as f:
+        f.write("// changed\n")
+    assert bench.stats_traffic(_w(base, "rejection_chain", 1)) is None  # the kernel changed since the capture
 
 
 def test_aux_modes_inputs_and_reference_arm(capsys):

@@ -24,6 +24,7 @@ _build.build()
 from reject_row_vocab_gb300 import device_workload as dw  # noqa: E402
 from reject_row_vocab_gb300 import specverify as sv  # noqa: E402
 from reject_row_vocab_gb300 import workload as wl  # noqa: E402
+from tests.gpu_compare import compare, oracle_outputs  # noqa: E402
 
 
 def _entry():
@@ -58,6 +59,38 @@ def test_no_alloc_entry_matches_workspace_entry_on_two_calls():
         got = out.to_numpy()
         for k, v in ref.items():
             assert np.array_equal(got[k], v), (w.name, k)
+        compare(w, got, oracle_outputs(w))
+
+
+def test_no_alloc_entry_clears_what_an_earlier_call_left():
+    """Each call clears the shared area's counter words itself: dirty counters (set on purpose, or left by a
+    call whose waits ran out) do not change the next call's results."""
+    fn = _entry()
+    lib = sv.load_library()
+    lib.spec_verify_noalloc_fill_counters.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    lib.spec_verify_set_hand_off_limit_ns.argtypes = [ctypes.c_uint64]
+    w = wl.rejection_chain(batch=12, m=7, vocab=20011, dtype="bf16", boost=2.0, seed=80, name="noalloc_dirty")
+    d = dw.DeviceInputs.from_workload(w)
+    want = oracle_outputs(w)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for value in (0xFF, 0x01):
+        assert lib.spec_verify_noalloc_fill_counters(value, stream) == 0
+        out = dw.outputs_for(w)
+        assert _call_noalloc(fn, w, d, out) == 0
+        torch.cuda.synchronize()
+        compare(w, out.to_numpy(), want)
+    assert lib.spec_verify_set_hand_off_limit_ns(2000) == 0
+    try:
+        out = dw.outputs_for(w)
+        assert _call_noalloc(fn, w, d, out) == 0
+        torch.cuda.synchronize()
+    finally:
+        lib.spec_verify_set_hand_off_limit_ns(0)
+    assert np.all(out.to_numpy()["status"] & 64)  # SV_DEV_TIMEOUT
+    out = dw.outputs_for(w)
+    assert _call_noalloc(fn, w, d, out) == 0
+    torch.cuda.synchronize()
+    compare(w, out.to_numpy(), want)
 
 
 def test_no_alloc_entry_rejects_sizes_beyond_its_scratch():
@@ -69,3 +102,14 @@ def test_no_alloc_entry_rejects_sizes_beyond_its_scratch():
     assert need > (4 << 20)
     # the size check happens before anything is read or enqueued
     assert _call_noalloc(fn, w, d, out, batch=4096, vocab=1 << 20) == 6  # SV_ERR_WORKSPACE_TOO_SMALL
+    # so do the argument checks: nothing of a refused call reaches the stream
+    out.commit_cu.fill_(-5)
+    st = out.struct()
+    null = None
+    assert fn(ctypes.c_void_p(d["logits"].data_ptr()), sv._dtype(d["logits"]), d["logits"].stride(0), w.batch,
+              w.max_len - 1, w.vocab, null, ctypes.c_void_p(d["q"].data_ptr()), d["q"].stride(0),
+              ctypes.c_void_p(d["temperature"].data_ptr()), ctypes.c_void_p(d["u_accept"].data_ptr()),
+              ctypes.c_void_p(d["u_final"].data_ptr()), null, null, ctypes.byref(st),
+              ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)) == 1  # SV_ERR_NULL_ARG
+    torch.cuda.synchronize()
+    assert np.all(out.commit_cu.cpu().numpy() == -5)
