@@ -390,9 +390,28 @@ __device__ __forceinline__ void fold_tail_probe(ThreadAcc& a, const LogitsView& 
   consume_dirty_probe<E>(a, x, static_cast<int32_t>(nfull), k, ik, d);
 }
 
+// NaN-propagating maximum of PER raw vectors (packed bf16 pairs reduced as pairs until the last step).
+template <int DT, int PER>
+__device__ __forceinline__ float raw_max_nan_n(const uint4 (&raw)[PER]) {
+  if constexpr (DT == SV_BF16) {
+    uint32_t w = bmax2_nan(bmax2_nan(raw[0].x, raw[0].y), bmax2_nan(raw[0].z, raw[0].w));
+#pragma unroll
+    for (int j = 1; j < PER; ++j)
+      w = bmax2_nan(w, bmax2_nan(bmax2_nan(raw[j].x, raw[j].y), bmax2_nan(raw[j].z, raw[j].w)));
+    return fmax_nan(bf16_lo(w), bf16_hi(w));
+  } else {
+    float m = raw_max_nan<DT>(raw[0]);
+#pragma unroll
+    for (int j = 1; j < PER; ++j) m = fmax_nan(m, raw_max_nan<DT>(raw[j]));
+    return m;
+  }
+}
+
 // Fold the first n vectors of a stage (vectors c0.. of the row).  A full
-// stage takes the thread's four vectors together: one check of their maximum
-// against the bound covers all four, then maxima and sums run branch-free.
+// stage takes the thread's four vectors together: one maximum over all four
+// (packed) is checked against the bound and against the running maximum;
+// only when the running maximum grows (rare after the first stages) is the
+// first vector holding it looked for.  The sums run branch-free.
 template <int DT, bool EXP, bool BELOW = false>
 __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
@@ -400,23 +419,21 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
   const int t = threadIdx.x;
   if (n == kChunkVecs) {
     uint4 raw[PER];
-    float vm[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) raw[j] = lds16(stage_addr + (t + j * kConsumers) * 16);
-#pragma unroll
-    for (int j = 0; j < PER; ++j) vm[j] = raw_max_nan<DT>(raw[j]);
-    float smax = vm[0];
-#pragma unroll
-    for (int j = 1; j < PER; ++j) smax = fmax_nan(smax, vm[j]);
+    const float smax = raw_max_nan_n<DT, PER>(raw);
     if (!(smax < a.bound)) {  // NaN / +inf, or the reference must move: vector by vector (rare)
 #pragma unroll
       for (int j = 0; j < PER; ++j) consume<DT, EXP, BELOW>(a, raw[j], c0 + t + j * kConsumers, k, ik);
       return;
     }
+    if (smax > a.m) {  // the first of the four vectors that reaches the new maximum
+      int32_t v = c0 + t + (PER - 1) * kConsumers;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      a.vidx = vm[j] > a.m ? c0 + t + j * kConsumers : a.vidx;
-      a.m = fmaxf(a.m, vm[j]);
+      for (int j = PER - 2; j >= 0; --j)
+        if (raw_max_nan<DT>(raw[j]) == smax) v = c0 + t + j * kConsumers;
+      a.vidx = v;
+      a.m = smax;
     }
     if (EXP) {
 #pragma unroll
