@@ -70,3 +70,13 @@ def test_aux_modes_inputs_and_reference_arm(capsys):
         line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
         assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
         assert line["metric"] == bench.AUX[kind]["metric"]
+
+
+def test_stats_event_slots():
+    import bench
+    assert bench.stats_event_slots(5, 1) == [0, 1, 2, 3, 4]
+    assert bench.stats_event_slots(25, 10) == [0] + [None] * 9 + [1] + [None] * 9 + [2] + [None] * 4
+    assert bench.stats_event_slots(3, 10) == [0, None, None]
+    slots = bench.stats_event_slots(100, 7)
+    used = [x for x in slots if x is not None]
+    assert used == list(range(len(used))) and len(used) == 15
