@@ -725,13 +725,22 @@ template <bool SP>
 __global__ void __launch_bounds__(kSampleThreads) k_draw(LogitsView lg, const float* q, int64_t ldq,
                                                          const float* u_final, OutView out, CommitParams cp, Ws ws,
                                                          int32_t excl_stride) {
-  grid_dependency_wait();  // the tile sums of k_sample
-  allow_dependents();
+  // The request's state, its row statistics and its uniform come from the kernels before k_sample, which had
+  // completed before any k_sample block passed its own dependency wait and let this grid start: they are read
+  // before waiting for the tile sums.
   const int b = blockIdx.x;
   const ReqState rq = ws.state[b];
-  if (!sampling_mode(rq.mode)) return;
-  const RowStat rs = ws.rowstat[rq.sample_row];
-  block_draw<false, SP>(lg, q, ldq, u_final[b], out, cp, ws, excl_stride, b, rq, rs);
+  const bool draws = sampling_mode(rq.mode);
+  RowStat rs{};
+  float u = 0.0f;
+  if (draws) {
+    rs = ws.rowstat[rq.sample_row];
+    u = u_final[b];
+  }
+  grid_dependency_wait();  // the tile sums of k_sample
+  allow_dependents();
+  if (!draws) return;
+  block_draw<false, SP>(lg, q, ldq, u, out, cp, ws, excl_stride, b, rq, rs);
 }
 
 __global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitParams cp) {
