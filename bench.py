@@ -30,9 +30,9 @@ if ROOT not in sys.path:
 
 METRIC = "verified rows/s"
 UNIT = "rows/s"
-# statistics, row merge, acceptance, then the commit alone (greedy) or the sampler (with the
-# commit) and the draws
-KERNELS_PER_STEP = {"greedy_chain": 4, "greedy_tree": 4, "rejection_chain": 5, "rejection_ragged": 5,
+# statistics, row merge, then for greedy calls of the benchmark's batch sizes (at most 32 requests) one kernel
+# that accepts and commits, else acceptance, the sampler (with the commit) and the draws
+KERNELS_PER_STEP = {"greedy_chain": 3, "greedy_tree": 3, "rejection_chain": 5, "rejection_ragged": 5,
                     "target_only_tree": 5, "rejection_chain_sparse": 5, "sample_match_chain": 5}
 STATS_SOURCES = ("reject_row_vocab_gb300/csrc/sv_stats.cu", "reject_row_vocab_gb300/csrc/sv_device.cuh")
 

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["sv_api.cu", "sv_stats.cu", "sv_accept.cu", "sv_sample.cu", "sv_noalloc.cu", "sv_sched.cu", "sv_tree_build.cu"]
-HEADERS = ["sv_internal.h", "sv_device.cuh"]
+HEADERS = ["sv_internal.h", "sv_device.cuh", "sv_commit.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

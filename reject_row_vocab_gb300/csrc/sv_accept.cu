@@ -17,6 +17,7 @@
 // and writes its accepted prefix straight into the outputs.
 #include <cstdint>
 
+#include "sv_commit.cuh"
 #include "sv_device.cuh"
 #include "sv_internal.h"
 
@@ -103,17 +104,12 @@ __device__ __forceinline__ int32_t write_sorted_candidates(const ChainParams& p,
   return n_valid;
 }
 
-__global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
-  // The inputs (ids, logits, q, uniforms) were complete before the statistics
-  // pass started, and this grid starts only after that pass: the gathers below
-  // are issued before waiting for the row statistics, overlapping that wait.
+// One chain request (b < p.batch) by one warp.  The inputs (ids, logits, q,
+// uniforms) were complete before the statistics pass started, and the calling
+// grid starts only after that pass: the gathers below are issued before
+// waiting for the row statistics, overlapping that wait.
+__device__ __forceinline__ void accept_chain_request(const ChainParams& p, const OutView& out, const Ws& ws, int b) {
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kChainWarps + (threadIdx.x >> 5);
-  if (b >= p.batch) {
-    grid_dependency_wait();
-    allow_dependents();
-    return;
-  }
   const int ML = p.max_len;
   int32_t* otok = out.out_tokens + static_cast<int64_t>(b) * ML;
   int32_t* orow = out.accept_rows + static_cast<int64_t>(b) * ML;
@@ -270,17 +266,14 @@ __global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p
   }
 }
 
-// One warp per request.  Node data is staged in shared memory.
-__global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, Ws ws) {
-  __shared__ int32_t s_tok[kMaxNodes];
-  __shared__ int32_t s_par[kMaxNodes];
-  __shared__ int32_t s_kid[kMaxNodes];
-  __shared__ float s_pk[kMaxNodes];
-  // Node data and the tree's validation come from inputs that were complete
-  // before the statistics pass started (this grid starts after that pass), so
-  // they are staged before waiting for the row statistics.
-  const int lane = threadIdx.x;
-  const int b = blockIdx.x;
+// One tree request (b < p.batch) by one warp, its node data staged in the
+// shared-memory arrays given (p.nodes entries each).  Node data and the tree's
+// validation come from inputs that were complete before the statistics pass
+// started (the calling grid starts after that pass), so they are staged before
+// waiting for the row statistics.
+__device__ __forceinline__ void accept_tree_request(const TreeParams& p, const OutView& out, const Ws& ws, int b,
+                                                    int32_t* s_tok, int32_t* s_par, int32_t* s_kid, float* s_pk) {
+  const int lane = threadIdx.x & 31;
   const int N = p.nodes;
   const int V = p.lg.vocab;
   const int64_t row0 = static_cast<int64_t>(b) * N;
@@ -439,7 +432,68 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
   }
 }
 
+__global__ void __launch_bounds__(32 * kChainWarps) k_accept_chain(ChainParams p, OutView out, Ws ws) {
+  const int b = blockIdx.x * kChainWarps + (threadIdx.x >> 5);
+  if (b >= p.batch) {
+    grid_dependency_wait();
+    allow_dependents();
+    return;
+  }
+  accept_chain_request(p, out, ws, b);
+}
+
+// One warp per request.  Node data is staged in shared memory.
+__global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, Ws ws) {
+  __shared__ int32_t s_tok[kMaxNodes];
+  __shared__ int32_t s_par[kMaxNodes];
+  __shared__ int32_t s_kid[kMaxNodes];
+  __shared__ float s_pk[kMaxNodes];
+  accept_tree_request(p, out, ws, blockIdx.x, s_tok, s_par, s_kid, s_pk);
+}
+
+// Greedy calls of a small batch: one CTA finishes every request (warp b takes
+// request b) and, once all are finished (a block barrier), writes the commit
+// lists with its first kCommitThreads threads, so the step needs no separate
+// commit launch.  Trees stage their node data in dynamic shared memory, four
+// arrays of p.nodes entries per warp.
+template <bool TREE>
+__global__ void __launch_bounds__(1024) k_accept_commit(ChainParams pc, TreeParams pt, OutView out, Ws ws,
+                                                       CommitParams cp) {
+  extern __shared__ int32_t s_nodes[];
+  const int warp = threadIdx.x >> 5;
+  const int B = TREE ? pt.batch : pc.batch;
+  if (warp < B) {
+    if constexpr (TREE) {
+      const int N = pt.nodes;
+      int32_t* base = s_nodes + static_cast<size_t>(warp) * 4 * N;
+      accept_tree_request(pt, out, ws, warp, base, base + N, base + 2 * N, reinterpret_cast<float*>(base + 3 * N));
+    } else {
+      accept_chain_request(pc, out, ws, warp);
+    }
+  }
+  __syncthreads();  // every request's outputs are written
+  if (threadIdx.x < kCommitThreads) commit_block_named(out, cp);
+}
+
 }  // namespace
+
+bool accept_commit_fits(int32_t batch, int32_t nodes) {
+  return batch >= 1 && batch <= kSmallGreedyBatch &&
+         (nodes <= 0 || int64_t{16} * nodes * batch <= kAcceptCommitSmemBytes);
+}
+
+cudaError_t launch_accept_commit_chain(const ChainParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
+                                       cudaStream_t stream) {
+  const int threads = 32 * p.batch > kCommitThreads ? 32 * p.batch : kCommitThreads;
+  return launch_pdl(k_accept_commit<false>, dim3(1), dim3(threads), 0, stream, p, TreeParams{}, out, ws, cp);
+}
+
+cudaError_t launch_accept_commit_tree(const TreeParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
+                                      cudaStream_t stream) {
+  const int threads = 32 * p.batch > kCommitThreads ? 32 * p.batch : kCommitThreads;
+  const size_t smem = size_t{16} * p.nodes * p.batch;
+  return launch_pdl(k_accept_commit<true>, dim3(1), dim3(threads), smem, stream, ChainParams{}, p, out, ws, cp);
+}
 
 cudaError_t launch_accept_chain(const ChainParams& p, const OutView& out, const Ws& ws, cudaStream_t stream) {
   const int blocks = (p.batch + kChainWarps - 1) / kChainWarps;

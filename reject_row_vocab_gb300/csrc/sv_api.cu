@@ -5,6 +5,7 @@
 // Launch sequences (each kernel chained to the previous one by programmatic
 // dependent launch):
 //   greedy chain / tree:          row stats -> row merge -> accept -> commit
+//     (batches of at most 32:     row stats -> row merge -> accept and commit in one CTA)
 //   rejection chain / ragged,
 //   sparse q, sample-then-match:  row stats -> row merge -> accept -> sample (tile sums; an extra block
 //                                 commits) -> draw
@@ -207,8 +208,13 @@ sv_status_t spec_verify_greedy_chain(const void* logits, sv_dtype_t dtype, int64
   ChainParams p{lg,      batch,   m + 1,   m + 1,   nullptr, verify_ids, nullptr, 0,
                 nullptr, nullptr, nullptr, nullptr, nullptr, 0,          0,       0};
   const OutView ov = out_view(out);
-  SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
-  SV_TRY_CUDA(launch_commit(ov, CommitParams{batch, m + 1, row_slots, seq_lens, w.err}, stream));
+  const CommitParams cp{batch, m + 1, row_slots, seq_lens, w.err};
+  if (accept_commit_fits(batch, 0)) {  // one CTA finishes and commits a small batch
+    SV_TRY_CUDA(launch_accept_commit_chain(p, ov, cp, w, stream));
+  } else {
+    SV_TRY_CUDA(launch_accept_chain(p, ov, w, stream));
+    SV_TRY_CUDA(launch_commit(ov, cp, stream));
+  }
   return SV_OK;
 }
 
@@ -379,8 +385,12 @@ static sv_status_t tree_common(int mode, const void* logits, sv_dtype_t dtype, i
                next_sibling, mode == 1 ? temperature : nullptr,
                threshold_single, threshold_acc,
                u_accept,    u_final};
-  SV_TRY_CUDA(launch_accept_tree(p, ov, w, stream));
   const CommitParams cp{batch, nodes, row_slots, seq_lens, w.err};
+  if (mode == 0 && accept_commit_fits(batch, nodes)) {  // one CTA walks and commits a small greedy batch
+    SV_TRY_CUDA(launch_accept_commit_tree(p, ov, cp, w, stream));
+    return SV_OK;
+  }
+  SV_TRY_CUDA(launch_accept_tree(p, ov, w, stream));
   if (mode == 1) {
     SV_TRY_CUDA(launch_sample_and_commit(lg, nullptr, 0, u_final, ov, cp, w, dev, stream));
   } else {

@@ -279,6 +279,16 @@ cudaError_t stats_occupancy(int dtype, int* blocks_per_sm);
 cudaError_t launch_accept_chain(const ChainParams& p, const OutView& out, const Ws& ws, cudaStream_t stream);
 cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws& ws, cudaStream_t stream);
 
+// Greedy calls of at most kSmallGreedyBatch requests (trees: node arrays within kAcceptCommitSmemBytes) are
+// finished and committed by one CTA, one warp per request, instead of the acceptance and commit kernels.
+constexpr int kSmallGreedyBatch = 32;
+constexpr int64_t kAcceptCommitSmemBytes = 48 * 1024;
+bool accept_commit_fits(int32_t batch, int32_t nodes);  // nodes <= 0: a chain
+cudaError_t launch_accept_commit_chain(const ChainParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
+                                       cudaStream_t stream);
+cudaError_t launch_accept_commit_tree(const TreeParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
+                                      cudaStream_t stream);
+
 // Residual / bonus sampler (two passes) followed by the commit, or the commit alone.
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,

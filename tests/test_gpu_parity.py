@@ -113,6 +113,17 @@ def test_tree_small(mode, V, keep):
     check(w, use_lists=True)
 
 
+@pytest.mark.parametrize("batch", [1, 32, 33, 70])
+def test_greedy_batch_sizes_around_the_single_cta_path(batch):
+    """Greedy calls of at most 32 requests are accepted and committed by one CTA; larger ones by the acceptance
+    and commit kernels: both match the oracle."""
+    check(wl.greedy_chain(batch=batch, m=5, vocab=3001, dtype="bf16", p_match=0.8, seed=batch))
+    w = wl.eagle2_tree(batch=batch, topk=3, depth=3, keep=8, vocab=2048, mode="greedy_tree", seed=batch + 1)
+    check(w)
+    w.first_child, w.next_sibling = wl.sibling_lists(w.parents)
+    check(w, use_lists=True)
+
+
 def test_chain_and_tree_entry_points_agree():
     w = wl.greedy_chain(batch=20, m=7, vocab=3000, dtype="bf16", p_match=0.85, seed=5)
     L = 8
