@@ -271,8 +271,12 @@ __device__ __forceinline__ void accept_chain_request(const ChainParams& p, const
 // validation come from inputs that were complete before the statistics pass
 // started (the calling grid starts after that pass), so they are staged before
 // waiting for the row statistics.
+// Sampling walks also stage, for every node, its token's logit under its
+// parent's row and the node's uniform (s_lg, s_u; NULL for greedy-only calls),
+// so a visited level waits only for its row statistics.
 __device__ __forceinline__ void accept_tree_request(const TreeParams& p, const OutView& out, const Ws& ws, int b,
-                                                    int32_t* s_tok, int32_t* s_par, int32_t* s_kid, float* s_pk) {
+                                                    int32_t* s_tok, int32_t* s_par, int32_t* s_kid, float* s_pk,
+                                                    float* s_lg, float* s_u) {
   const int lane = threadIdx.x & 31;
   const int N = p.nodes;
   const int V = p.lg.vocab;
@@ -312,6 +316,14 @@ __device__ __forceinline__ void accept_tree_request(const TreeParams& p, const O
 
   const float T = p.temperature ? p.temperature[b] : 0.0f;
   const bool greedy = !sampling_temperature(T);
+  if (!greedy && s_lg) {
+    for (int i = lane; i < N; i += 32) {
+      const int32_t pi = s_par[i], t = s_tok[i];
+      s_lg[i] = (!bad && i > 0 && t >= 0 && t < V) ? load_logit(p.lg, row0 + pi, t) : 0.0f;
+      s_u[i] = p.u_accept[row0 + i];
+    }
+    __syncwarp();
+  }
   grid_dependency_wait();  // row statistics from the previous kernel
   allow_dependents();
   uint32_t st = (bad ? kStBadTree : 0u) | (__ldcg(ws.err) ? kStTimeout : 0u);
@@ -373,11 +385,11 @@ __device__ __forceinline__ void accept_tree_request(const TreeParams& p, const O
     } else {
       for (int kk = lane; kk < nk; kk += 32) {
         const int32_t t = s_tok[s_kid[kk]];
-        s_pk[kk] = (t >= 0 && t < V) ? target_prob(load_logit(p.lg, row, t), rs) : 0.0f;
+        s_pk[kk] = (t >= 0 && t < V) ? target_prob(s_lg ? s_lg[s_kid[kk]] : load_logit(p.lg, row, t), rs) : 0.0f;
       }
       __syncwarp();
       if (lane == 0) {
-        const float u = p.u_accept[row];
+        const float u = s_u ? s_u[cur] : p.u_accept[row];
         float c = 0.0f;
         int32_t* excl = ws.excl + static_cast<int64_t>(b) * N;
         for (int kk = 0; kk < nk; ++kk) {
@@ -448,7 +460,9 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
   __shared__ int32_t s_par[kMaxNodes];
   __shared__ int32_t s_kid[kMaxNodes];
   __shared__ float s_pk[kMaxNodes];
-  accept_tree_request(p, out, ws, blockIdx.x, s_tok, s_par, s_kid, s_pk);
+  __shared__ float s_lg[kMaxNodes];
+  __shared__ float s_u[kMaxNodes];
+  accept_tree_request(p, out, ws, blockIdx.x, s_tok, s_par, s_kid, s_pk, s_lg, s_u);
 }
 
 // Greedy calls of a small batch: one CTA finishes every request (warp b takes
@@ -466,7 +480,8 @@ __global__ void __launch_bounds__(1024) k_accept_commit(ChainParams pc, TreePara
     if constexpr (TREE) {
       const int N = pt.nodes;
       int32_t* base = s_nodes + static_cast<size_t>(warp) * 4 * N;
-      accept_tree_request(pt, out, ws, warp, base, base + N, base + 2 * N, reinterpret_cast<float*>(base + 3 * N));
+      accept_tree_request(pt, out, ws, warp, base, base + N, base + 2 * N, reinterpret_cast<float*>(base + 3 * N),
+                          nullptr, nullptr);  // greedy calls only
     } else {
       accept_chain_request(pc, out, ws, warp);
     }
