@@ -305,9 +305,15 @@ def time_oracle(w, seconds: float, threads: int) -> dict:
         el = time.perf_counter() - t0
         if el >= seconds:
             break
+    if w.kind == "sample_match_chain":  # plain Python over the C++ row statistics: one host thread
+        threads, how = 1, "Python loop over requests on one thread"
+    elif w.kind == "rejection_chain_sparse":
+        how = "candidate lists scattered by numpy on one thread, then std::thread over requests"
+    else:
+        how = "std::thread over requests"
     return {"value": w.rows * reps / el, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "full batch (%d requests, %d rows) x %d repetitions, std::thread over requests"
-                      % (w.batch, w.rows, reps), "seconds": round(el, 3)}
+            "sample": "full batch (%d requests, %d rows) x %d repetitions, %s" % (w.batch, w.rows, reps, how),
+            "seconds": round(el, 3)}
 
 
 def step_parity(w, res: dict, threads: int) -> dict:
