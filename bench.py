@@ -256,6 +256,46 @@ L2_BYTES = 129e6
 FLUSH_BYTES = 256 << 20  # about twice the L2
 
 
+def event_context(logits, flush_l2, cap, pairs: int = 20, replays: int = 5):
+    """The statistics kernel's timing, applied to two other kernels in the same setting (the same L2 flush before
+    each, the same event nodes in a CUDA graph when the bench uses one): an empty kernel, whose span is the fixed
+    cost of the timing itself, and torch.sum over the same logits, what a plain library reduction reaches on the
+    same bytes.  Medians in us; None when this torch cannot record event nodes inside a graph."""
+    import torch
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+               for _ in range(pairs)]
+    except TypeError:
+        return None
+    kernels = {"empty_kernel_us": lambda: torch.cuda._sleep(0),
+               "torch_sum_us": lambda: torch.sum(logits, dtype=torch.float32)}
+    res = {}
+    for name, fn in kernels.items():
+        def body():
+            for a, b in evs:
+                if flush_l2 is not None:
+                    flush_l2()
+                a.record()
+                fn()
+                b.record()
+        if cap is not None:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                body()
+            run = g.replay
+        else:
+            run = body
+        run()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(replays):
+            run()
+            torch.cuda.synchronize()
+            ts += [a.elapsed_time(b) * 1e3 for a, b in evs]
+        res[name] = statistics.median(ts)
+    return res
+
+
 def stats_event_slots(n: int, every: int) -> list:
     """For each of n launches, the index of the event pair recorded around its row-statistics kernel, or None:
     one launch in `every` (the first of each group) is instrumented, so most steps run without event nodes."""
@@ -452,6 +492,7 @@ def run_ours(args):
         elapsed_s -= f0.elapsed_time(f1) / 1e3
     max_s = ranks.max(elapsed_s)
     avg_stats_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs)  # last recording of each pair
+    floor = event_context(d["logits"], flush_l2 if flush else None, None if graph is None else cap)
 
     res = out.to_numpy()
     committed = int(res["num_out"].sum())
@@ -513,7 +554,9 @@ def run_ours(args):
                                    % ("every launch" if E == 1 else "one launch in %d; the others run without "
                                                                         "event nodes" % E),
                      "bytes_per_launch": alg_bytes,
-                     "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src},
+                     "avg_launch_us": avg_stats_ms * 1e3, "peak_source": peak_src,
+                     "event_context": None if floor is None else dict(
+                         floor, torch_sum_frac=alg_bytes / (floor["torch_sum_us"] * 1e-6) / 1e9 / peak)},
         "clocks": clk, "gpu_launches": KERNELS_PER_STEP[w.kind] * launched,
         "e2e": e2e, "cpu_baseline": cpu, "parity": parity,
         "inputs_sha256": w.sha256(),  # first 16 hex digits per input array (rank 0's batch)
