@@ -410,8 +410,9 @@ __device__ __forceinline__ float raw_max_nan_n(const uint4 (&raw)[PER]) {
 // Fold the first n vectors of a stage (vectors c0.. of the row).  A full
 // stage takes the thread's four vectors together: one maximum over all four
 // (packed) is checked against the bound and against the running maximum;
-// only when the running maximum grows (rare after the first stages) is the
-// first vector holding it looked for.  The sums run branch-free.
+// when it reaches the bound the reference moves once, to that maximum; only
+// when the running maximum grows (rare after the first stages) is the first
+// vector holding it looked for.  The sums run branch-free.
 template <int DT, bool EXP, bool BELOW = false>
 __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
@@ -422,10 +423,15 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
 #pragma unroll
     for (int j = 0; j < PER; ++j) raw[j] = lds16(stage_addr + (t + j * kConsumers) * 16);
     const float smax = raw_max_nan_n<DT, PER>(raw);
-    if (!(smax < a.bound)) {  // NaN / +inf, or the reference must move: vector by vector (rare)
+    if (!(smax < a.bound)) {
+      if (!EXP || !(smax < kInfF)) {  // NaN / +inf present: vector by vector (rare)
 #pragma unroll
-      for (int j = 0; j < PER; ++j) consume<DT, EXP, BELOW>(a, raw[j], c0 + t + j * kConsumers, k, ik);
-      return;
+        for (int j = 0; j < PER; ++j) consume<DT, EXP, BELOW>(a, raw[j], c0 + t + j * kConsumers, k, ik);
+        return;
+      }
+      // The reference moves (a chunk's first stage, or a logit far above the running maximum, frequent at low
+      // temperatures): once, to the stage maximum, so every term of the stage is at most 1.
+      move_ref(a, smax, k, ik);
     }
     if (smax > a.m) {  // the first of the four vectors that reaches the new maximum
       int32_t v = c0 + t + (PER - 1) * kConsumers;
