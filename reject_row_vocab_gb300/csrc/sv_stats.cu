@@ -253,8 +253,7 @@ __device__ __forceinline__ float2 exp_sum(const float (&x)[E], float k, float R)
 
 // Fold E logits one at a time, NaN and +inf entries read as -inf (the caller
 // flags them).
-// BELOW: the vectors lie wholly below the row's probe token: their terms also go to a.sb.
-template <int E, bool EXP, bool BELOW = false>
+template <int E, bool EXP>
 __device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E], int32_t vec, float k, float ik) {
   for (int i = 0; i < E; ++i) {
     const float v = usable_logit(x[i]) ? x[i] : -kInfF;
@@ -264,16 +263,14 @@ __device__ __forceinline__ void consume_dirty(ThreadAcc& a, const float (&x)[E],
     }
     if (EXP) {
       if (v >= a.bound) move_ref(a, v, k, ik);
-      const float t = ex2_fast(fmaf(v, k, -a.R));
-      a.s.x += t;
-      if (BELOW) a.sb += t;
+      a.s.x += ex2_fast(fmaf(v, k, -a.R));
     }
   }
 }
 
 // Fold one vector.  The common case (clean data, maximum below the bound) is
 // branch-free.
-template <int DT, bool EXP, bool BELOW = false>
+template <int DT, bool EXP>
 __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
   float x[E];
@@ -282,7 +279,7 @@ __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t 
   if (!(vmax < a.bound)) {  // NaN / +inf present, or the reference must move (rare)
     if (!(vmax < kInfF)) {
       a.flags |= kStNonFinite;
-      consume_dirty<E, EXP, BELOW>(a, x, vec, k, ik);
+      consume_dirty<E, EXP>(a, x, vec, k, ik);
       return;
     }
     if (EXP) move_ref(a, vmax, k, ik);
@@ -291,9 +288,7 @@ __device__ __forceinline__ void consume(ThreadAcc& a, const uint4& raw, int32_t 
   a.vidx = raised ? vec : a.vidx;
   a.m = fmaxf(a.m, vmax);
   if (EXP) {
-    const float2 es = exp_sum<E>(x, k, a.R);
-    a.s = __fadd2_rn(a.s, es);
-    if (BELOW) a.sb += es.x + es.y;
+    a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
   }
 }
 
@@ -315,23 +310,10 @@ __device__ __forceinline__ void consume_dirty_probe(ThreadAcc& a, const float (&
   }
 }
 
-template <int DT>
-__device__ __forceinline__ void consume_probe(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik,
-                                              int32_t d) {
-  constexpr int E = VecTraits<DT>::E;
-  float x[E];
-  unpack<DT>(raw, x);
-  const float vmax = raw_max_nan<DT>(raw);
-  if (!(vmax < a.bound)) {
-    if (!(vmax < kInfF)) {
-      a.flags |= kStNonFinite;
-      consume_dirty_probe<E>(a, x, vec, k, ik, d);
-      return;
-    }
-    move_ref(a, vmax, k, ik);
-  }
-  a.vidx = vmax > a.m ? vec : a.vidx;
-  a.m = fmaxf(a.m, vmax);
+// The terms of one clean vector (maximum below the bound), those of ids below d also to a.sb.
+template <int E>
+__device__ __forceinline__ void probe_vector_terms(ThreadAcc& a, const float (&x)[E], int32_t vec, float k,
+                                                   int32_t d) {
   const float2 kk = make_float2(k, k), nR = make_float2(-a.R, -a.R);
   float t[E];
 #pragma unroll
@@ -351,14 +333,23 @@ __device__ __forceinline__ void consume_probe(ThreadAcc& a, const uint4& raw, in
 }
 
 template <int DT>
-__device__ __forceinline__ void fold_stage_probe(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k,
-                                                 float ik, int32_t d) {
-  constexpr int PER = kChunkVecs / kConsumers;
-#pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int vi = threadIdx.x + j * kConsumers;
-    if (vi < n) consume_probe<DT>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik, d);
+__device__ __forceinline__ void consume_probe(ThreadAcc& a, const uint4& raw, int32_t vec, float k, float ik,
+                                              int32_t d) {
+  constexpr int E = VecTraits<DT>::E;
+  float x[E];
+  unpack<DT>(raw, x);
+  const float vmax = raw_max_nan<DT>(raw);
+  if (!(vmax < a.bound)) {
+    if (!(vmax < kInfF)) {
+      a.flags |= kStNonFinite;
+      consume_dirty_probe<E>(a, x, vec, k, ik, d);
+      return;
+    }
+    move_ref(a, vmax, k, ik);
   }
+  a.vidx = vmax > a.m ? vec : a.vidx;
+  a.m = fmaxf(a.m, vmax);
+  probe_vector_terms<E>(a, x, vec, k, d);
 }
 
 // The row's ragged tail (vocab not a multiple of the vector width) as vector nfull, by one thread.
@@ -413,7 +404,7 @@ __device__ __forceinline__ float raw_max_nan_n(const uint4 (&raw)[PER]) {
 // when it reaches the bound the reference moves once, to that maximum; only
 // when the running maximum grows (rare after the first stages) is the first
 // vector holding it looked for.  The sums run branch-free.
-template <int DT, bool EXP, bool BELOW = false>
+template <int DT, bool EXP>
 __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k, float ik) {
   constexpr int E = VecTraits<DT>::E;
   constexpr int PER = kChunkVecs / kConsumers;  // vectors per consumer thread per full stage
@@ -426,7 +417,7 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
     if (!(smax < a.bound)) {
       if (!EXP || !(smax < kInfF)) {  // NaN / +inf present: vector by vector (rare)
 #pragma unroll
-        for (int j = 0; j < PER; ++j) consume<DT, EXP, BELOW>(a, raw[j], c0 + t + j * kConsumers, k, ik);
+        for (int j = 0; j < PER; ++j) consume<DT, EXP>(a, raw[j], c0 + t + j * kConsumers, k, ik);
         return;
       }
       // The reference moves (a chunk's first stage, or a logit far above the running maximum, frequent at low
@@ -446,16 +437,67 @@ __device__ __forceinline__ void fold_stage(ThreadAcc& a, uint32_t stage_addr, in
       for (int j = 0; j < PER; ++j) {
         float x[E];
         unpack<DT>(raw[j], x);
-        const float2 es = exp_sum<E>(x, k, a.R);
-        a.s = __fadd2_rn(a.s, es);
-        if (BELOW) a.sb += es.x + es.y;
+        a.s = __fadd2_rn(a.s, exp_sum<E>(x, k, a.R));
       }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
       const int vi = t + j * kConsumers;
-      if (vi < n) consume<DT, EXP, BELOW>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik);
+      if (vi < n) consume<DT, EXP>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik);
+    }
+  }
+}
+
+// The stage holding the probe's vector pv = d / E: folded like any full stage,
+// and the terms of vectors below pv, and of the ids below d inside pv (one
+// thread's vector), also go to a.sb.  A partial stage goes vector by vector.
+template <int DT>
+__device__ __forceinline__ void fold_stage_probe(ThreadAcc& a, uint32_t stage_addr, int32_t c0, int n, float k,
+                                                 float ik, int32_t d) {
+  constexpr int E = VecTraits<DT>::E;
+  constexpr int PER = kChunkVecs / kConsumers;
+  const int t = threadIdx.x;
+  const int32_t pv = d / E;
+  if (n == kChunkVecs) {
+    uint4 raw[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) raw[j] = lds16(stage_addr + (t + j * kConsumers) * 16);
+    const float smax = raw_max_nan_n<DT, PER>(raw);
+    if (!(smax < a.bound)) {
+      if (!(smax < kInfF)) {  // NaN / +inf present: vector by vector
+#pragma unroll
+        for (int j = 0; j < PER; ++j) consume_probe<DT>(a, raw[j], c0 + t + j * kConsumers, k, ik, d);
+        return;
+      }
+      move_ref(a, smax, k, ik);
+    }
+    if (smax > a.m) {
+      int32_t v = c0 + t + (PER - 1) * kConsumers;
+#pragma unroll
+      for (int j = PER - 2; j >= 0; --j)
+        if (raw_max_nan<DT>(raw[j]) == smax) v = c0 + t + j * kConsumers;
+      a.vidx = v;
+      a.m = smax;
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int32_t vec = c0 + t + j * kConsumers;
+      float x[E];
+      unpack<DT>(raw[j], x);
+      if (vec != pv) {
+        const float2 es = exp_sum<E>(x, k, a.R);
+        a.s = __fadd2_rn(a.s, es);
+        if (vec < pv) a.sb += es.x + es.y;
+      } else {
+        probe_vector_terms<E>(a, x, vec, k, d);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int vi = t + j * kConsumers;
+      if (vi < n) consume_probe<DT>(a, lds16(stage_addr + vi * 16), c0 + vi, k, ik, d);
     }
   }
 }
@@ -859,12 +901,12 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
     if (k > 0.0f) {
       ThreadAcc a = acc_init<true>();  // one partial per chunk: independent of the schedule
       for (int32_t s = 0;; ++s) {
-        // In the probe chunk only the stage holding the probe's vector goes
-        // vector by vector; stages wholly below it add their sums to sb too.
+        // In the probe chunk, every term folded before the stage holding the
+        // probe's vector lies below the probe: sb starts there as the running
+        // sum, and that stage adds its own terms below the probe.
         const int64_t pv = PFX && pd >= 0 ? pd / E : -1;
-        if (PFX && pd >= 0 && md.c0 + md.n <= pv) {
-          fold_stage<DT, true, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
-        } else if (PFX && pd >= 0 && md.c0 <= pv) {
+        if (PFX && pd >= 0 && md.c0 <= pv && pv < md.c0 + md.n) {
+          a.sb = a.s.x + a.s.y;
           fold_stage_probe<DT>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik, pd);
         } else {
           fold_stage<DT, true>(a, smem_addr(&sm.buf[st][0]), md.c0, md.n, k, ik);
@@ -880,6 +922,7 @@ __global__ void __launch_bounds__(kStatsThreads, 3) k_row_stats(LogitsView lg, R
         }
         md = sm.meta[st];
       }
+      if (PFX && pd >= 0 && pd / E >= nfull) a.sb = a.s.x + a.s.y;  // the probe is in the ragged tail
       if (tail && threadIdx.x == 0) {
         if (PFX && pd >= 0) {
           fold_tail_probe<DT>(a, lg, row, nfull, k, ik, pd);

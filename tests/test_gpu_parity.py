@@ -75,6 +75,38 @@ def test_row_stats_and_probabilities(dtype, rows, V):
     assert np.all(np.abs(p - ref["p"]) <= 2e-6 * np.maximum(ref["p"], 1e-30) + 1e-12)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("with_probe", [False, True])
+@pytest.mark.parametrize("V", [4099, 151936])
+def test_row_stats_extreme_temperatures(dtype, with_probe, V):
+    # Low temperatures move the exponent reference often (the bound sits 16/k logits above it), high ones never;
+    # wide rows make l*k large.  Z must stay within 2e-6 of the fp64 oracle, max and argmax exact.
+    rng = np.random.default_rng(V + (7 if with_probe else 0) + (1 if dtype == "bf16" else 0))
+    temps = [0.01, 0.05, 0.25, 0.5, 1.0, 4.0, 100.0]
+    rows = 2 * len(temps) + 2
+    x = (rng.standard_normal((rows, V)) * 3).astype(np.float32)
+    x[len(temps):2 * len(temps)] *= 20.0  # wide rows: logits up to about +-250
+    x[-2] = 1.5  # all equal: Z = V exactly
+    x[-1] = -np.inf
+    x[-1, V // 3] = 2.0  # a single usable entry: Z = 1
+    logits = wl.f32_to_bf16_bits(x) if dtype == "bf16" else x
+    T = np.array(temps * 2 + [0.3, 0.3], dtype=np.float32)
+    probe = rng.integers(0, V, rows).astype(np.int32) if with_probe else None
+    ref = oracle.row_stats(logits, dtype, row_temp=T, probe=probe)
+    t = dw.padded_rows(dw._to_tensor(logits), "cuda")
+    r = sv.row_stats(t, row_temp=torch.from_numpy(T).cuda(),
+                     probe=torch.from_numpy(probe).cuda() if with_probe else None)
+    torch.cuda.synchronize()
+    assert np.array_equal(r["argmax"].cpu().numpy(), ref["argmax"])
+    assert np.array_equal(r["max"].cpu().numpy().astype(np.float64), ref["max"])
+    z = r["z"].cpu().numpy()
+    assert np.all(np.abs(z - ref["z"]) <= 2e-6 * ref["z"]), np.max(np.abs(z - ref["z"]) / ref["z"])
+    assert z[-2] == V and z[-1] == 1.0
+    if with_probe:
+        p = r["p"].cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(p - ref["p"]) <= 2e-6 * np.maximum(ref["p"], 1e-30) + 1e-12)
+
+
 # ---------------------------------------------------------------------------
 # Small cases spanning several tiles and a ragged tail
 # ---------------------------------------------------------------------------
