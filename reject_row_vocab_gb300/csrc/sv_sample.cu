@@ -465,6 +465,7 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
 constexpr int kSampleStages = 3;
 constexpr int kSampleStageBytes = 32 * 1024;
 constexpr int kSampleStageMaxTiles = 32;
+constexpr int kSampleBlocksPerSM = 2;
 constexpr uint64_t kSampleWaitNs = 1000000000ull;
 constexpr int kSampleBlockThreads = kSampleThreads + 32;  // consumers + one producer warp
 constexpr size_t kSampleSmemBytes = static_cast<size_t>(kSampleStages) * kSampleStageBytes + 256;
@@ -481,8 +482,35 @@ __device__ __forceinline__ int stage_tiles(int dtype, bool resid) {
   return n < kSampleStageMaxTiles ? n : kSampleStageMaxTiles;
 }
 
+// Tile sums of one landed stage holding n tiles from tile c0 of the sampled row,
+// by the eight consumer warps: logits at src and, for a residual draw, q at
+// src + lb.  Specialised on the logits type and the draw, so no unused loads
+// or branches stay live (excluded-token draws take the general path).
+template <int DT, bool RESID>
+__device__ __forceinline__ void stage_tile_sums(uint32_t src, uint32_t lb, int n, int c0, const RowStat& rs,
+                                                float inv_z, uint64_t* ts) {
+  constexpr int ES = DT == SV_BF16 ? 2 : 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < n; i += kSampleWarps) {
+    const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
+    LaneRaw raw;
+    raw.l0 = lds16(src + off * ES);
+    if (ES == 4) raw.l1 = lds16(src + off * ES + 16);
+    if (RESID) {
+      raw.q0 = lds16(src + lb + off * 4);
+      raw.q1 = lds16(src + lb + off * 4 + 16);
+    }
+    float x[8], qv[8], w[8];
+    lane_unpack(raw, DT, RESID, x, qv);
+    weights_from_values<false>(x, qv, rs, inv_z, RESID ? kModeResidual : kModeP, nullptr, nullptr, 0,
+                               static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+    const uint64_t fa = warp_sum_u64(to_fixed(lane_sum(w)));
+    if (lane == 0) ts[c0 + i] = fa;
+  }
+}
+
 template <bool SP>
-__global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg, const float* q, int64_t ldq,
+__global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sample(LogitsView lg, const float* q, int64_t ldq,
                                                                    const float* u_final, OutView out,
                                                                    CommitParams cp, Ws ws, int32_t excl_stride,
                                                                    int32_t nblocks) {
@@ -617,11 +645,21 @@ __global__ void __launch_bounds__(kSampleBlockThreads, 2) k_sample(LogitsView lg
               if (i2 < n) ts[c0 + i2] = fc;
             }
           }
-        } else {  // dense q: the q loads already fill the registers; one tile at a time
+        } else if (rq.mode == kModePExcl) {  // excluded tokens: the general weights
           for (int i = warp; i < n; i += kSampleWarps) {
             const uint64_t fa = warp_sum_u64(tile_sum(i));
             if (lane == 0) ts[c0 + i] = fa;
           }
+        } else if (lg.dtype == SV_BF16) {
+          if (resid) {
+            stage_tile_sums<SV_BF16, true>(smem_addr(src), lb, n, c0, rs, inv_z, ts);
+          } else {
+            stage_tile_sums<SV_BF16, false>(smem_addr(src), lb, n, c0, rs, inv_z, ts);
+          }
+        } else if (resid) {
+          stage_tile_sums<SV_F32, true>(smem_addr(src), lb, n, c0, rs, inv_z, ts);
+        } else {
+          stage_tile_sums<SV_F32, false>(smem_addr(src), lb, n, c0, rs, inv_z, ts);
         }
       }
       __syncwarp();
@@ -681,9 +719,10 @@ cudaError_t sample_smem_setup() {
 cudaError_t launch_sample_and_commit(const LogitsView& lg, const float* q, int64_t ldq, const float* u_final,
                                      const OutView& out, const CommitParams& cp, const Ws& ws,
                                      const DeviceInfo& dev, cudaStream_t stream, bool sparse_q) {
-  // one resident wave (two blocks per SM, one slot for the commit block), at least ~16 tiles per block
+  // one resident wave (kSampleBlocksPerSM blocks per SM, one slot for the commit block), at least ~16 tiles per
+  // block
   const int64_t tiles = static_cast<int64_t>(cp.batch) * ws.ntiles;
-  int64_t nblocks = static_cast<int64_t>(dev.sms) * 2 - 1;
+  int64_t nblocks = static_cast<int64_t>(dev.sms) * kSampleBlocksPerSM - 1;
   if (nblocks > (tiles + 15) / 16) nblocks = (tiles + 15) / 16;
   if (nblocks < 1) nblocks = 1;
   const cudaError_t e =
