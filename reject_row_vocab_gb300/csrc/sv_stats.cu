@@ -16,7 +16,8 @@
 // stages into a four-stage shared-memory ring with bulk copies (the TMA
 // engine; completion counted on an mbarrier per stage), eight consumer warps
 // fold each stage with packed fp32x2 arithmetic against an exponent reference
-// that moves only when a logit grows 16 log2 units past it, and at the end of
+// that moves only when a logit grows 16 log2 units past it (then once, to the
+// stage's maximum, so the stage stays on the packed path), and at the end of
 // a chunk each warp combines its lanes and hands the result to a finalizer
 // warp, which finds the chunk's argmax element in the one vector the warp
 // results point to and writes the chunk's partial (maximum, its lowest index,
