@@ -516,12 +516,13 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
                                                                    int32_t nblocks) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ SampleRing ring;
-  grid_dependency_wait();  // acceptance results from the previous kernel
-  allow_dependents();
   if (blockIdx.x == 0) {  // the commit block (first, so it runs in the first wave)
+    grid_dependency_wait();  // acceptance results from the previous kernel
+    allow_dependents();
     if (threadIdx.x < kCommitThreads) commit_block_named(out, cp);
     return;
   }
+  // The block's tile range and its ring depend on nothing the previous kernels write: set up before waiting.
   const int64_t blk = blockIdx.x - 1;
   unsigned char* stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                            ~uintptr_t(127));
@@ -531,6 +532,7 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
   const int64_t total = static_cast<int64_t>(cp.batch) * T;
   const int64_t t_begin = blk * total / nblocks, t_end = (blk + 1) * total / nblocks;
   if (t_begin >= t_end) return;
+  const int64_t b_first = t_begin / T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSampleStages; ++i) {
@@ -541,11 +543,13 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
     mbar_fence_init();
   }
   __syncthreads();
+  grid_dependency_wait();  // acceptance results from the previous kernel
+  allow_dependents();
 
   if (warp == kSampleWarps) {  // ------------------------------------------ producer
     if (lane == 0) {
       uint32_t g = 0;
-      for (int64_t b = t_begin / T; b * T < t_end && !ring.abort; ++b) {
+      for (int64_t b = b_first; b * T < t_end && !ring.abort; ++b) {
         const int ta = static_cast<int>((t_begin > b * T ? t_begin : b * T) - b * T);
         const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
         const ReqState rq = ws.state[b];
@@ -587,7 +591,7 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
 
   // -------------------------------------------------------------------- consumers
   uint32_t g = 0;
-  for (int64_t b = t_begin / T; b * T < t_end; ++b) {
+  for (int64_t b = b_first; b * T < t_end; ++b) {
     const int ta = static_cast<int>((t_begin > b * T ? t_begin : b * T) - b * T);
     const int tb = static_cast<int>((t_end < (b + 1) * T ? t_end : (b + 1) * T) - b * T);
     const ReqState rq = ws.state[b];
