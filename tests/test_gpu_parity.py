@@ -135,6 +135,15 @@ def test_ragged_small(V):
     check(w1)
 
 
+@pytest.mark.parametrize("batch", [511, 512, 2000])
+def test_ragged_batch_around_the_staged_table_size(batch):
+    # Up to 511 requests the statistics kernel stages the request offsets (batch + 1 entries) and temperatures in
+    # shared memory; beyond, each chunk's row finds its request by searching cu_seqlens in global memory.
+    w = wl.ragged_block(batch=batch, max_len=8, vocab=4099, seed=batch + 5)
+    g, o, res = check(w)
+    assert res["requests"] == batch
+
+
 @pytest.mark.parametrize("mode", ["greedy_tree", "target_only_tree"])
 @pytest.mark.parametrize("V,keep", [(64, 6), (2000, 16), (5003, 30)])
 def test_tree_small(mode, V, keep):
