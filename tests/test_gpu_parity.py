@@ -145,6 +145,16 @@ def test_ragged_batch_around_the_staged_table_size(batch):
 
 
 @pytest.mark.parametrize("mode", ["greedy_tree", "target_only_tree"])
+@pytest.mark.parametrize("batch,topk,depth,keep", [(4, 16, 16, 256), (12, 16, 16, 256), (6, 8, 16, 128)])
+def test_tree_large(mode, batch, topk, depth, keep):
+    # 129 and 257 nodes per request; greedy batches whose node arrays fit the one-CTA accept-and-commit kernel
+    # (4 x 257 nodes) and batches that do not (12 x 257 nodes) take different kernels.
+    w = wl.eagle2_tree(batch=batch, topk=topk, depth=depth, keep=keep, vocab=2048, mode=mode, noise_sigma=0.5,
+                       seed=batch * 100 + keep, name="tree_large_%s_%d" % (mode, keep + 1))
+    check(w)
+
+
+@pytest.mark.parametrize("mode", ["greedy_tree", "target_only_tree"])
 @pytest.mark.parametrize("V,keep", [(64, 6), (2000, 16), (5003, 30)])
 def test_tree_small(mode, V, keep):
     w = wl.eagle2_tree(batch=12, topk=3, depth=4, keep=keep, vocab=V, mode=mode, noise_sigma=0.5,
