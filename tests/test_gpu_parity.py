@@ -145,7 +145,8 @@ def test_ragged_batch_around_the_staged_table_size(batch):
 
 
 @pytest.mark.parametrize("mode", ["greedy_tree", "target_only_tree"])
-@pytest.mark.parametrize("batch,topk,depth,keep", [(4, 16, 16, 256), (12, 16, 16, 256), (6, 8, 16, 128)])
+@pytest.mark.parametrize("batch,topk,depth,keep", [(4, 16, 16, 256), (12, 16, 16, 256), (6, 8, 16, 128),
+                                                   (2, 32, 40, 1023)])  # the last: the 1024-node maximum
 def test_tree_large(mode, batch, topk, depth, keep):
     # 129 and 257 nodes per request; greedy batches whose node arrays fit the one-CTA accept-and-commit kernel
     # (4 x 257 nodes) and batches that do not (12 x 257 nodes) take different kernels.
