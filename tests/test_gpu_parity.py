@@ -48,7 +48,8 @@ def check(w, use_lists=False):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("rows,V", [(4, 1), (5, 3), (3, 7), (9, 16), (7, 1000), (33, 4099), (2, 151936),
-                                    (3000, 64), (5, 32000)])
+                                    (3000, 64), (5, 32000),
+                                    (40, 262147)])  # 33 (bf16) or 64 (fp32) one-stage chunks per tail row
 def test_row_stats_and_probabilities(dtype, rows, V):
     rng = np.random.default_rng(rows * 1000 + V)
     x = (rng.standard_normal((rows, V)) * 3).astype(np.float32)
@@ -133,6 +134,14 @@ def test_ragged_small(V):
     check(w)
     w1 = wl.ragged_block(lens=[1, 1, 3, 1, 8], max_len=8, vocab=V, seed=V + 3)  # bonus-only requests
     check(w1)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rejection_chain_more_than_32_chunks_per_row(dtype):
+    # V = 262147: tail rows hold 33 (bf16) or 64 (fp32) chunks, so the row merge's lanes fold several each
+    w = wl.rejection_chain(batch=8, m=7, vocab=262147, dtype=dtype, seed=262 + (dtype == "bf16"),
+                           name="chain_v262147_" + dtype)
+    check(w)
 
 
 @pytest.mark.parametrize("batch", [511, 512, 2000])
