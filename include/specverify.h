@@ -192,8 +192,12 @@ sv_status_t spec_verify_sample_match_chain(const void* logits, sv_dtype_t dtype,
  * cand_ids[i][c] == v.  Id -1 is padding; any other id outside [0, vocab) is
  * ignored and sets SV_DEV_TOKEN_RANGE for the request when it appears in one of
  * the request's tested rows (all rows but its last).  No dense q is read or
- * formed.  ws: at least spec_verify_sparse_workspace_bytes(batch * (m + 1),
- * batch, vocab, m + 1, num_cands) bytes (same rules as every workspace).
+ * formed; the final draw of a rejected request reads that row's list in place,
+ * so the lists, like every input, must stay unchanged until the call's work on
+ * the stream has completed.  ws: at least
+ * spec_verify_sparse_workspace_bytes(batch * (m + 1), batch, vocab, m + 1,
+ * num_cands) bytes (same rules as every workspace; num_cands does not change
+ * the size).
  */
 size_t spec_verify_sparse_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len,
                                           int32_t num_cands);

@@ -60,50 +60,6 @@ __device__ __forceinline__ float sparse_q_at(const ChainParams& p, int64_t row, 
   return q;
 }
 
-// The candidates of a sparse residual row, valid ids only, sorted by id (equal
-// ids keep their candidate order), into the request's workspace list; returns
-// their number.  The whole warp takes part.
-__device__ __forceinline__ int32_t write_sorted_candidates(const ChainParams& p, int64_t row, int32_t* cid,
-                                                           float* cq) {
-  const int lane = threadIdx.x & 31;
-  const int32_t* ids = p.cand_ids + row * p.ldc;
-  const float* pr = p.cand_probs + row * p.ldc;
-  const int K = p.num_cands, V = p.lg.vocab;
-  int32_t n_valid = 0;
-  if (K <= 32) {  // one candidate per lane: ranks from shuffles, no reloads
-    const int32_t id = lane < K ? ids[lane] : -1;
-    const float pv = lane < K ? pr[lane] : 0.0f;
-    const bool ok = lane < K && id >= 0 && id < V;
-    n_valid = __popc(__ballot_sync(kFull, ok));
-    int rank = 0;  // valid candidates ordered before this one (by id, then position)
-    for (int o = 0; o < 32; ++o) {
-      const int32_t oid = __shfl_sync(kFull, id, o);
-      const bool ook = o < K && oid >= 0 && oid < V;
-      if (ook && (oid < id || (oid == id && o < lane))) ++rank;
-    }
-    if (ok) {
-      cid[rank] = id;
-      cq[rank] = pv;
-    }
-    return n_valid;
-  }
-  for (int c0 = 0; c0 < K; c0 += 32) {
-    const int c = c0 + lane;
-    const int32_t id = c < K ? ids[c] : -1;
-    n_valid += __popc(__ballot_sync(kFull, c < K && id >= 0 && id < V));
-    if (c < K && id >= 0 && id < V) {
-      int rank = 0;  // valid candidates ordered before this one
-      for (int o = 0; o < K; ++o) {
-        const int32_t oid = ids[o];
-        if (oid >= 0 && oid < V && (oid < id || (oid == id && o < c))) ++rank;
-      }
-      cid[rank] = id;
-      cq[rank] = pr[c];
-    }
-  }
-  return n_valid;
-}
-
 // One chain request (b < p.batch) by one warp.  The inputs (ids, logits, q,
 // uniforms) were complete before the statistics pass started, and the calling
 // grid starts only after that pass: the gathers below are issued before
@@ -240,10 +196,8 @@ __device__ __forceinline__ void accept_chain_request(const ChainParams& p, const
     // sample-then-match: the final row is drawn from its own p with its own uniform
     mode = (how == 1 && !p.match) ? (sparse ? kModeResidualSparse : kModeResidual) : kModeP;
   }
-  int32_t n_list = 0;
-  if (mode == kModeResidualSparse)
-    n_list = write_sorted_candidates(p, fr, ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap,
-                                     ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap);
+  // a sparse residual draw reads row fr's candidate list in place, all num_cands entries
+  const int32_t n_list = mode == kModeResidualSparse ? p.num_cands : 0;
   for (int64_t k = lane; k < ML; k += 32) {
     int32_t t = -1, r = -1;
     if (k < s) {

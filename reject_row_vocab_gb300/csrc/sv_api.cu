@@ -77,9 +77,8 @@ sv_status_t check_out(const sv_out_t* out, const int64_t* row_slots, const int64
   return SV_OK;
 }
 
-sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, Ws* w,
-                  int32_t num_cands = 0) {
-  const WsLayout L = ws_layout(rows, batch, vocab, max_len, num_cands);
+sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, Ws* w) {
+  const WsLayout L = ws_layout(rows, batch, vocab, max_len);
   if (!ws || ws_bytes < L.total || !aligned(ws, 256)) return SV_ERR_WORKSPACE_TOO_SMALL;
   char* base = static_cast<char*>(ws);
   w->done_cnt = reinterpret_cast<uint32_t*>(base + L.done_cnt);
@@ -90,9 +89,6 @@ sv_status_t carve(void* ws, size_t ws_bytes, int64_t rows, int32_t batch, int32_
   w->ureq = reinterpret_cast<float*>(base + L.ureq);
   w->state = reinterpret_cast<ReqState*>(base + L.state);
   w->excl = reinterpret_cast<int32_t*>(base + L.excl);
-  w->cand_id = reinterpret_cast<int32_t*>(base + L.cand);
-  w->cand_q = reinterpret_cast<float*>(base + L.cand + 4 * static_cast<size_t>(batch > 0 ? batch : 1) * L.cand_cap);
-  w->cand_cap = L.cand_cap;
   w->tsum = reinterpret_cast<uint64_t*>(base + L.tsum);
   w->ntiles = L.ntiles;
   return SV_OK;
@@ -239,12 +235,14 @@ static sv_status_t rejection_common(const void* logits, sv_dtype_t dtype, int64_
   }
   SV_TRY(check_out(out, row_slots, seq_lens));
   Ws w{};
-  SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w, cand_ids ? num_cands : 0));
+  SV_TRY(carve(ws, ws_bytes, rows, batch, vocab, max_len, &w));
+  w.cand_id = cand_ids;  // the final draws read the residual row's list in place
+  w.cand_q = cand_probs;
+  w.cand_ld = ldc;
   DeviceInfo dev{};
   SV_TRY_CUDA(device_info(&dev));
   if (clear_counters)
-    SV_TRY_CUDA(cudaMemsetAsync(w.done_cnt, 0, ws_layout(rows, batch, vocab, max_len, cand_ids ? num_cands : 0).counters_end,
-                                stream));
+    SV_TRY_CUDA(cudaMemsetAsync(w.done_cnt, 0, ws_layout(rows, batch, vocab, max_len).counters_end, stream));
   const LogitsView lg{logits, dtype, ld, rows, vocab};
   const OutView ov = out_view(out);
   if (rows > 0) {
@@ -321,8 +319,8 @@ sv_status_t spec_verify_sample_match_chain(const void* logits, sv_dtype_t dtype,
 }
 
 size_t spec_verify_sparse_workspace_bytes(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len,
-                                          int32_t num_cands) {
-  return ws_layout(rows, batch, vocab, max_len, num_cands).total;
+                                          int32_t /*num_cands*/) {
+  return ws_layout(rows, batch, vocab, max_len).total;  // the candidate lists are read in place
 }
 
 sv_status_t spec_verify_rejection_chain_sparse(const void* logits, sv_dtype_t dtype, int64_t ld, int32_t batch,

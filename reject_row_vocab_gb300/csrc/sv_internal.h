@@ -81,14 +81,13 @@ constexpr int kMaxNodes = 1024;
 
 struct WsLayout {
   size_t done_cnt, counters_end;
-  size_t rowstat, partial, psb, state, excl, cand, ureq, tsum, total;
-  int32_t cand_cap;  // candidate-list entries per request (sparse q), at least 1
+  size_t rowstat, partial, psb, state, excl, ureq, tsum, total;
   int32_t ntiles;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len, int32_t num_cands = 0) {
+inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t max_len) {
   WsLayout L{};
   size_t off = 0;
   L.done_cnt = off;
@@ -112,9 +111,6 @@ inline WsLayout ws_layout(int64_t rows, int32_t batch, int32_t vocab, int32_t ma
                            static_cast<size_t>(max_len > 0 ? max_len : 1), 256);
   L.ureq = off;  // per request: the uniform of its final draw when it differs from u_final
   off = align_up(off + sizeof(float) * static_cast<size_t>(batch > 0 ? batch : 1), 256);
-  L.cand = off;  // per request: the residual row's candidates sorted by id (id, probability)
-  L.cand_cap = num_cands > 0 ? num_cands : 1;
-  off = align_up(off + 8 * static_cast<size_t>(batch > 0 ? batch : 1) * static_cast<size_t>(L.cand_cap), 256);
   L.ntiles = (vocab + kTile - 1) / kTile;
   L.tsum = off;
   off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(batch > 0 ? batch : 1) *
@@ -133,9 +129,9 @@ struct Ws {
   float* ureq;  // per request: the uniform of the final draw (sample-then-match)
   ReqState* state;
   int32_t* excl;
-  int32_t* cand_id;  // [B, cand_cap] sorted candidate ids of a sparse residual row
-  float* cand_q;     // [B, cand_cap] their probabilities
-  int32_t cand_cap;
+  const int32_t* cand_id;  // sparse q: the caller's candidate lists [rows, cand_ld], read in place
+  const float* cand_q;     // their probabilities
+  int64_t cand_ld;
   uint64_t* tsum;  // fixed-point tile sums of the sampled rows
   int32_t ntiles;
 };

@@ -89,29 +89,30 @@ __device__ __forceinline__ void lane_unpack(const LaneRaw& r, int32_t dtype, boo
 }
 
 // A sparse residual row's first 32 candidates held in registers, one per
-// lane (loaded once per request; later entries are read from memory).
+// lane (loaded once per request; later entries are read from memory).  The
+// list is the caller's, in candidate order; an id outside [0, V) (padding -1
+// included) is held as -1 and never matches an entry.
 struct CandRegs {
   int32_t id;
   float q;
 };
 
-__device__ __forceinline__ CandRegs load_cand_regs(const int32_t* cid, const float* cq, int32_t n) {
+__device__ __forceinline__ CandRegs load_cand_regs(const int32_t* cid, const float* cq, int32_t n, int32_t V) {
   const int lane = threadIdx.x & 31;
-  return CandRegs{lane < n ? cid[lane] : -1, lane < n ? cq[lane] : 0.0f};
+  const int32_t id = lane < n ? cid[lane] : -1;
+  return CandRegs{id >= 0 && id < V ? id : -1, lane < n ? cq[lane] : 0.0f};
 }
 
 // Weights of eight entries from their values; the single definition both
 // passes use, so a tile's weights are bit-identical in both.
-// SP: the kernel serves sparse-q requests (kModeResidualSparse); without it
-// that mode is compiled out.  For kModePExcl (excl, n_excl) lists the tokens to zero; for
-// kModeResidualSparse (excl, excl_q, n_excl) is the row's candidate list
-// sorted by id, and w = max(p - q, 0) with q the list's probabilities,
-// subtracted in list order.
+// SP: the kernel serves sparse-q requests; a dense residual is compiled out of
+// it.  For kModePExcl (excl, n_excl) lists the tokens to zero.  A sparse
+// residual (kModeResidualSparse) takes p here (mode kModeP) and its
+// candidates from apply_candidates_tile.
 template <bool SP>
 __device__ __forceinline__ void weights_from_values(const float (&x)[8], const float (&qv)[8], const RowStat& rs,
-                                                    float inv_z, int32_t mode, const int32_t* excl,
-                                                    const float* excl_q, int32_t n_excl, int64_t col0,
-                                                    float (&w)[8], const CandRegs& cr = CandRegs{-1, 0.0f}) {
+                                                    float inv_z, int32_t mode, const int32_t* excl, int32_t n_excl,
+                                                    int64_t col0, float (&w)[8]) {
   // Packed pairs: each lane of a pair rounds exactly like the scalar
   // operation, so w_i = fl(fl(ex2(fl(fl(x_i - M) * k)) / Z) - q_i) either way.
   const float2 nM = make_float2(-rs.M, -rs.M), kk = make_float2(rs.k, rs.k), iz = make_float2(inv_z, inv_z);
@@ -137,34 +138,22 @@ __device__ __forceinline__ void weights_from_values(const float (&x)[8], const f
       for (int i = 0; i < 8; ++i)
         if (d == i) w[i] = 0.0f;
     }
-  } else if (SP && mode == kModeResidualSparse) {  // whole warp: the first 32 entries come by shuffle
-    for (int e = 0; e < n_excl; ++e) {
-      const int32_t id = e < 32 ? __shfl_sync(0xffffffffu, cr.id, e) : excl[e];
-      const float qe = e < 32 ? __shfl_sync(0xffffffffu, cr.q, e) : excl_q[e];
-      const int64_t d = static_cast<int64_t>(id) - col0;
-      if (d >= 0 && d < 8) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (d == i) w[i] = __fsub_rn(w[i], qe);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = fmaxf(w[i], 0.0f);
   }
 }
 
-// The same candidate subtraction for a whole tile [t0, t0 + 256) at once: the
-// warp finds the (rare) candidates inside the tile with a ballot and the
-// owning lane subtracts them, in list order, so the result equals the lane
-// loop of weights_from_values exactly.  w holds p on entry.
+// The residual of a sparse q over a whole tile [t0, t0 + 256), the whole
+// warp taking part: w = max(p - q, 0), where q at an entry is subtracted once
+// per candidate carrying its id, in candidate order.  The warp finds the
+// (rare) candidates inside the tile with a ballot and the owning lane
+// subtracts them.  Ids outside [0, V) are ignored.  w holds p on entry.
 __device__ __forceinline__ void apply_candidates_tile(float (&w)[8], int64_t t0, int lane, const int32_t* cid,
-                                                      const float* cq, int32_t n, const CandRegs& cr) {
+                                                      const float* cq, int32_t n, int32_t V, const CandRegs& cr) {
   for (int g = 0; g < n; g += 32) {
     const int c = g + lane;
     const int32_t id = g == 0 ? cr.id : (c < n ? cid[c] : -1);
     const float qq = g == 0 ? cr.q : (c < n ? cq[c] : 0.0f);
     const int64_t off = static_cast<int64_t>(id) - t0;
-    unsigned hit = __ballot_sync(0xffffffffu, c < n && off >= 0 && off < kTile);
+    unsigned hit = __ballot_sync(0xffffffffu, c < n && id < V && off >= 0 && off < kTile);
     while (hit) {
       const int src = __ffs(hit) - 1;
       hit &= hit - 1;
@@ -182,7 +171,8 @@ __device__ __forceinline__ void apply_candidates_tile(float (&w)[8], int64_t t0,
 }
 
 // The eight weights of one lane of a tile: entries [col0, col0 + 8) of `row`.
-// Entries past the vocabulary weigh 0.
+// Entries past the vocabulary weigh 0.  A sparse residual (SP) needs the
+// whole warp on one tile, lane l at col0 = tile start + 8 l.
 template <bool SP>
 __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* q, int64_t ldq, int64_t row,
                                              const RowStat& rs, float inv_z, int32_t mode, const int32_t* excl,
@@ -202,7 +192,12 @@ __device__ __forceinline__ void lane_weights(const LogitsView& lg, const float* 
       qv[i] = (resid && in) ? __ldg(q + row * ldq + col0 + i) : 0.0f;
     }
   }
-  weights_from_values<SP>(x, qv, rs, inv_z, mode, excl, excl_q, n_excl, col0, w, cr);
+  const bool sparse = SP && mode == kModeResidualSparse;
+  weights_from_values<SP>(x, qv, rs, inv_z, sparse ? kModeP : mode, excl, n_excl, col0, w);
+  if (sparse) {
+    const int lane = threadIdx.x & 31;
+    apply_candidates_tile(w, col0 - lane * 8, lane, excl, excl_q, n_excl, lg.vocab, cr);
+  }
 }
 
 // A lane's weight sum: fp32, left to right.  Pass B walks the same additions.
@@ -258,8 +253,8 @@ __device__ __forceinline__ void warp_tile_sums_t(const LogitsView& lg, const flo
         }
         float x[8], qv[8], w[8];
         lane_unpack(r, DT, RESID, x, qv);
-        weights_from_values<false>(x, qv, rs, inv_z, mode, excl, nullptr, n_excl,
-                            static_cast<int64_t>(t0 + u) * kTile + lane * 8, w);
+        weights_from_values<false>(x, qv, rs, inv_z, mode, excl, n_excl, static_cast<int64_t>(t0 + u) * kTile + lane * 8,
+                                   w);
         ls[u] = lane_sum(w);
       }
     } else {
@@ -313,11 +308,13 @@ __device__ __forceinline__ void warp_tile_sums(const LogitsView& lg, const float
 // The draw of one request by one CTA, once all its tile sums exist: scan the
 // (exact, fixed-point) tile sums, pick the tile holding T = floor(u_final * S),
 // then one warp re-forms that tile's weights (same arithmetic as the sums) and
-// walks to the entry.  rs is the sampled row's statistics, u its uniform.
+// walks to the entry.  rs is the sampled row's statistics, u its uniform, cr
+// the first candidates of a sparse residual row (load_cand_regs).
 template <bool NAMED, bool SP>
 __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q, int64_t ldq, float u,
                                            const OutView& out, const CommitParams& cp, const Ws& ws,
-                                           int32_t excl_stride, int b, const ReqState& rq, const RowStat& rs) {
+                                           int32_t excl_stride, int b, const ReqState& rq, const RowStat& rs,
+                                           const CandRegs& cr) {
   __shared__ uint64_t s_scan[kSampleWarps + 1];
   __shared__ int s_tile;
   __shared__ int s_last_nz;
@@ -327,9 +324,8 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
   const int64_t row = rq.sample_row;
   const float inv_z = inverse_z(rs);
   const bool sparse = SP && rq.mode == kModeResidualSparse;
-  const int32_t* excl = sparse ? ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap
-                               : ws.excl + static_cast<int64_t>(b) * excl_stride;
-  const float* excl_q = sparse ? ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap : nullptr;
+  const int32_t* excl = sparse ? ws.cand_id + row * ws.cand_ld : ws.excl + static_cast<int64_t>(b) * excl_stride;
+  const float* excl_q = sparse ? ws.cand_q + row * ws.cand_ld : nullptr;
   uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
   int32_t mode = rq.mode;
   uint32_t st_add = 0u;
@@ -412,8 +408,6 @@ __device__ __forceinline__ void block_draw(const LogitsView& lg, const float* q,
     const uint64_t tpre = located ? s_pre : 0;
     const int64_t col0 = static_cast<int64_t>(tile) * kTile + lane * 8;
     float w[8];
-    const CandRegs cr = (SP && mode == kModeResidualSparse) ? load_cand_regs(excl, excl_q, rq.n_excl)
-                                                            : CandRegs{-1, 0.0f};
     lane_weights<SP>(lg, q, ldq, row, rs, inv_z, mode, excl, excl_q,
                      (mode == kModePExcl || mode == kModeResidualSparse) ? rq.n_excl : 0, col0, w, cr);
     const uint64_t W = to_fixed(lane_sum(w));
@@ -502,10 +496,51 @@ __device__ __forceinline__ void stage_tile_sums(uint32_t src, uint32_t lb, int n
     }
     float x[8], qv[8], w[8];
     lane_unpack(raw, DT, RESID, x, qv);
-    weights_from_values<false>(x, qv, rs, inv_z, RESID ? kModeResidual : kModeP, nullptr, nullptr, 0,
+    weights_from_values<false>(x, qv, rs, inv_z, RESID ? kModeResidual : kModeP, nullptr, 0,
                                static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
     const uint64_t fa = warp_sum_u64(to_fixed(lane_sum(w)));
     if (lane == 0) ts[c0 + i] = fa;
+  }
+}
+
+// The fixed-point weight sum of tile i of a stage holding a sparse residual
+// row from tile c0 (logits only; p minus the candidate list cid / cq of nc
+// entries, the first 32 in cr), summed over the lane's eight entries only.
+template <int DT>
+__device__ __forceinline__ uint64_t sparse_lane_fx(uint32_t src, int i, int c0, const RowStat& rs, float inv_z,
+                                                   const int32_t* cid, const float* cq, int32_t nc, int32_t V,
+                                                   const CandRegs& cr) {
+  constexpr int ES = DT == SV_BF16 ? 2 : 4;
+  const int lane = threadIdx.x & 31;
+  const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
+  LaneRaw raw;
+  raw.l0 = lds16(src + off * ES);
+  if (ES == 4) raw.l1 = lds16(src + off * ES + 16);
+  float x[8], qv[8], w[8];
+  lane_unpack(raw, DT, false, x, qv);
+  weights_from_values<true>(x, qv, rs, inv_z, kModeP, nullptr, 0, static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+  apply_candidates_tile(w, static_cast<int64_t>(c0 + i) * kTile, lane, cid, cq, nc, V, cr);
+  return to_fixed(lane_sum(w));
+}
+
+// Tile sums of one landed stage of a sparse residual row.  Two tiles per warp
+// and iteration, so their dependency chains (weights, candidates, lane sum,
+// fixed-point conversion, warp reduction) overlap.
+template <int DT>
+__device__ __forceinline__ void stage_tile_sums_sparse(uint32_t src, int n, int c0, const RowStat& rs, float inv_z,
+                                                       const int32_t* cid, const float* cq, int32_t nc, int32_t V,
+                                                       const CandRegs& cr, uint64_t* ts) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < n; i += 2 * kSampleWarps) {
+    const int i2 = i + kSampleWarps;
+    const uint64_t a = sparse_lane_fx<DT>(src, i, c0, rs, inv_z, cid, cq, nc, V, cr);
+    const uint64_t c = i2 < n ? sparse_lane_fx<DT>(src, i2, c0, rs, inv_z, cid, cq, nc, V, cr) : 0ull;
+    const uint64_t fa = warp_sum_u64(a);  // i2 < n is the same in every lane
+    const uint64_t fc = warp_sum_u64(c);
+    if (lane == 0) {
+      ts[c0 + i] = fa;
+      if (i2 < n) ts[c0 + i2] = fc;
+    }
   }
 }
 
@@ -603,10 +638,9 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
     const RowStat rs = ws.rowstat[row];
     const float inv_z = inverse_z(rs);
     const bool sparse = SP && rq.mode == kModeResidualSparse;
-    const int32_t* excl = sparse ? ws.cand_id + static_cast<int64_t>(b) * ws.cand_cap
-                                 : ws.excl + static_cast<int64_t>(b) * excl_stride;
-    const float* excl_q = sparse ? ws.cand_q + static_cast<int64_t>(b) * ws.cand_cap : nullptr;
-    const CandRegs cr = sparse ? load_cand_regs(excl, excl_q, rq.n_excl) : CandRegs{-1, 0.0f};
+    const int32_t* excl = sparse ? ws.cand_id + row * ws.cand_ld : ws.excl + static_cast<int64_t>(b) * excl_stride;
+    const float* excl_q = sparse ? ws.cand_q + row * ws.cand_ld : nullptr;
+    const CandRegs cr = sparse ? load_cand_regs(excl, excl_q, rq.n_excl, lg.vocab) : CandRegs{-1, 0.0f};
     uint64_t* ts = ws.tsum + static_cast<int64_t>(b) * T;
     for (int c0 = ta; c0 < tc; c0 += per, ++g) {
       const int n = min(per, tc - c0);
@@ -617,41 +651,25 @@ __global__ void __launch_bounds__(kSampleBlockThreads, kSampleBlocksPerSM) k_sam
         ring.abort = 1;
         atomicOr(ws.err, 1u);
       } else {
-        // Sparse q: two tiles per warp and iteration, so their dependency
-        // chains (weights, lane sum, fixed-point conversion, warp reduction)
-        // overlap.
-        auto tile_sum = [&](int i) -> uint64_t {
-          const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
-          LaneRaw r;
-          r.l0 = lds16(smem_addr(src) + off * es);
-          if (es == 4) r.l1 = lds16(smem_addr(src) + off * es + 16);
-          if (resid) {
-            r.q0 = lds16(smem_addr(src + lb) + off * 4);
-            r.q1 = lds16(smem_addr(src + lb) + off * 4 + 16);
+        if (SP && sparse) {
+          if (lg.dtype == SV_BF16) {
+            stage_tile_sums_sparse<SV_BF16>(smem_addr(src), n, c0, rs, inv_z, excl, excl_q, rq.n_excl, lg.vocab, cr,
+                                            ts);
+          } else {
+            stage_tile_sums_sparse<SV_F32>(smem_addr(src), n, c0, rs, inv_z, excl, excl_q, rq.n_excl, lg.vocab, cr,
+                                           ts);
           }
-          float x[8], qv[8], w[8];
-          lane_unpack(r, lg.dtype, resid, x, qv);
-          weights_from_values<SP>(x, qv, rs, inv_z, sparse ? kModeP : rq.mode, excl, excl_q, rq.n_excl,
-                                  static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
-          if (SP && sparse)
-            apply_candidates_tile(w, static_cast<int64_t>(c0 + i) * kTile, lane, excl, excl_q, rq.n_excl, cr);
-          return to_fixed(lane_sum(w));
-        };
-        if constexpr (SP) {
-          for (int i = warp; i < n; i += 2 * kSampleWarps) {
-            const int i2 = i + kSampleWarps;
-            const uint64_t a = tile_sum(i);
-            const uint64_t c = i2 < n ? tile_sum(i2) : 0ull;  // i2 < n is the same in every lane
-            const uint64_t fa = warp_sum_u64(a);
-            const uint64_t fc = warp_sum_u64(c);
-            if (lane == 0) {
-              ts[c0 + i] = fa;
-              if (i2 < n) ts[c0 + i2] = fc;
-            }
-          }
-        } else if (rq.mode == kModePExcl) {  // excluded tokens: the general weights
+        } else if (!SP && rq.mode == kModePExcl) {  // excluded tokens: the general weights
           for (int i = warp; i < n; i += kSampleWarps) {
-            const uint64_t fa = warp_sum_u64(tile_sum(i));
+            const uint32_t off = static_cast<uint32_t>(i) * kTile + lane * 8;  // element offset in the stage
+            LaneRaw r;
+            r.l0 = lds16(smem_addr(src) + off * es);
+            if (es == 4) r.l1 = lds16(smem_addr(src) + off * es + 16);
+            float x[8], qv[8], w[8];
+            lane_unpack(r, lg.dtype, false, x, qv);
+            weights_from_values<SP>(x, qv, rs, inv_z, kModePExcl, excl, rq.n_excl,
+                                    static_cast<int64_t>(c0 + i) * kTile + lane * 8, w);
+            const uint64_t fa = warp_sum_u64(to_fixed(lane_sum(w)));
             if (lane == 0) ts[c0 + i] = fa;
           }
         } else if (lg.dtype == SV_BF16) {
@@ -687,21 +705,25 @@ __global__ void __launch_bounds__(kSampleThreads) k_draw(LogitsView lg, const fl
                                                          const float* u_final, OutView out, CommitParams cp, Ws ws,
                                                          int32_t excl_stride) {
   // The request's state, its row statistics and its uniform come from the kernels before k_sample, which had
-  // completed before any k_sample block passed its own dependency wait and let this grid start: they are read
-  // before waiting for the tile sums.
+  // completed before any k_sample block passed its own dependency wait and let this grid start, and a sparse
+  // row's candidates are inputs: all are read before waiting for the tile sums.
   const int b = blockIdx.x;
   const ReqState rq = ws.state[b];
   const bool draws = sampling_mode(rq.mode);
   RowStat rs{};
   float u = 0.0f;
+  CandRegs cr{-1, 0.0f};
   if (draws) {
     rs = ws.rowstat[rq.sample_row];
     u = u_final[b];
+    if (SP && rq.mode == kModeResidualSparse && threadIdx.x < 32)
+      cr = load_cand_regs(ws.cand_id + rq.sample_row * ws.cand_ld, ws.cand_q + rq.sample_row * ws.cand_ld,
+                          rq.n_excl, lg.vocab);
   }
   grid_dependency_wait();  // the tile sums of k_sample
   allow_dependents();
   if (!draws) return;
-  block_draw<false, SP>(lg, q, ldq, u, out, cp, ws, excl_stride, b, rq, rs);
+  block_draw<false, SP>(lg, q, ldq, u, out, cp, ws, excl_stride, b, rq, rs, cr);
 }
 
 __global__ void __launch_bounds__(kCommitThreads) k_commit(OutView out, CommitParams cp) {

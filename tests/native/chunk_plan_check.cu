@@ -25,19 +25,17 @@ static int check_ws_layout() {
   const int32_t batches[] = {0, 1, 8, 64, 256, 4096};
   const int32_t vocabs[] = {1, 3, 1000, 32000, 151936, 262144};
   const int32_t maxlens[] = {1, 5, 16, 1024};
-  const int32_t cands[] = {0, 1, 16, 1024};
   for (int64_t R : rowss)
     for (int32_t B : batches)
       for (int32_t V : vocabs)
-        for (int32_t ML : maxlens)
-          for (int32_t K : cands) {
-            const WsLayout L = ws_layout(R, B, V, ML, K);
+        for (int32_t ML : maxlens) {
+            const WsLayout L = ws_layout(R, B, V, ML);
             ++cases;
             const size_t r1 = R > 0 ? R : 1, b1 = B > 0 ? B : 1, m1 = ML > 0 ? ML : 1;
             const size_t nfull = (V > 0 ? V : 1) / 4;
             const size_t cpr = nfull >= 1 ? (nfull + 1023) / 1024 : 1;  // chunks per row, 1024-vector chunks
             const size_t starts[] = {L.done_cnt, L.counters_end, L.rowstat, L.partial, L.psb, L.state, L.excl,
-                                     L.ureq, L.cand, L.tsum, L.total};
+                                     L.ureq, L.tsum, L.total};
             bool ok = L.done_cnt == 0 && L.counters_end >= 16 && L.rowstat >= L.counters_end;
             for (size_t i = 1; i < sizeof(starts) / sizeof(starts[0]); ++i)
               ok = ok && starts[i] % 256 == 0 && starts[i] >= starts[i - 1];
@@ -46,13 +44,12 @@ static int check_ws_layout() {
             ok = ok && L.state - L.psb >= sizeof(float) * r1 * cpr;
             ok = ok && L.excl - L.state >= sizeof(ReqState) * b1;
             ok = ok && L.ureq - L.excl >= sizeof(int32_t) * b1 * m1;
-            ok = ok && L.cand - L.ureq >= sizeof(float) * b1;
-            ok = ok && L.cand_cap >= (K > 0 ? K : 1) && L.tsum - L.cand >= 8 * b1 * static_cast<size_t>(L.cand_cap);
+            ok = ok && L.tsum - L.ureq >= sizeof(float) * b1;
             ok = ok && L.ntiles == (V + kTile - 1) / kTile &&
                  L.total - L.tsum >= sizeof(uint64_t) * b1 * static_cast<size_t>(L.ntiles > 0 ? L.ntiles : 1);
             if (!ok) {
               if (bad < 10)
-                std::printf("ws layout: R=%lld B=%d V=%d ML=%d K=%d\n", (long long)R, B, V, ML, K);
+                std::printf("ws layout: R=%lld B=%d V=%d ML=%d\n", (long long)R, B, V, ML);
               ++bad;
             }
           }

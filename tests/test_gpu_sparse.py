@@ -62,9 +62,18 @@ def test_sparse_degenerate_inputs():
     T[4] = 0.0                          # greedy request among sampling ones
     T[5] = float("nan")                 # greedy too
     pr[6 * L:7 * L] *= 0.5              # q need not sum to 1
+    # request 7 rejects its first draft (q(d) huge) and its residual row lists ids past V and below -1 with
+    # negative probabilities: both are ignored, so no weight appears outside the vocabulary
+    r = 7 * L
+    d = w.verify_ids[r + 1]
+    pr[r, ids[r] == d] = 1e6
+    ids[r, 6], pr[r, 6] = w.vocab + 5, -1.0  # inside the last (ragged) tile
+    ids[r, 7], pr[r, 7] = -3, -1.0
     w2 = dataclasses.replace(w, cand_ids=ids, cand_probs=pr, temperature=T)
     g, o = check(w2)
     assert (int(g["status"][1]) & 1) == 1 and (int(g["status"][2]) & 1) == 0
+    assert int(o["accept_len"][7]) == 0 and (int(g["status"][7]) & 1) == 1
+    assert 0 <= int(g["bonus"][7]) < w.vocab
 
 
 def test_full_size_sparse_dflash_block():
