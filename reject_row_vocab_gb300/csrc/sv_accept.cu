@@ -423,13 +423,24 @@ __global__ void __launch_bounds__(32) k_accept_tree(TreeParams p, OutView out, W
 // request b) and, once all are finished (a block barrier), writes the commit
 // lists with its first kCommitThreads threads, so the step needs no separate
 // commit launch.  Trees stage their node data in dynamic shared memory, four
-// arrays of p.nodes entries per warp.
+// arrays of p.nodes entries per warp.  The KV slots of up to kStagedSlots rows
+// and the sequence lengths (inputs) are staged in shared memory before the
+// dependency wait, so the commit gathers them without a memory round trip.
+constexpr int kStagedSlots = 1024;
+
 template <bool TREE>
 __global__ void __launch_bounds__(1024) k_accept_commit(ChainParams pc, TreeParams pt, OutView out, Ws ws,
                                                        CommitParams cp) {
   extern __shared__ int32_t s_nodes[];
+  __shared__ int64_t s_slots[kStagedSlots];
+  __shared__ int64_t s_seq[kSmallGreedyBatch];
   const int warp = threadIdx.x >> 5;
   const int B = TREE ? pt.batch : pc.batch;
+  const int64_t rows = TREE ? pt.lg.rows : pc.lg.rows;
+  const bool stage_slots = cp.row_slots && out.commit_src_slot && rows <= kStagedSlots;
+  const bool stage_seq = cp.seq_lens && out.commit_dst_pos;
+  for (int64_t i = threadIdx.x; stage_slots && i < rows; i += blockDim.x) s_slots[i] = cp.row_slots[i];
+  if (stage_seq && threadIdx.x < B) s_seq[threadIdx.x] = cp.seq_lens[threadIdx.x];
   if (warp < B) {
     if constexpr (TREE) {
       const int N = pt.nodes;
@@ -440,11 +451,18 @@ __global__ void __launch_bounds__(1024) k_accept_commit(ChainParams pc, TreePara
       accept_chain_request(pc, out, ws, warp);
     }
   }
-  __syncthreads();  // every request's outputs are written
-  if (threadIdx.x < kCommitThreads) commit_block_named(out, cp);
+  __syncthreads();  // every request's outputs are written (and the staged slots)
+  if (threadIdx.x < kCommitThreads)
+    commit_block_named(out, cp, stage_slots ? s_slots : nullptr, stage_seq ? s_seq : nullptr);
 }
 
 }  // namespace
+
+cudaError_t accept_smem_setup() {
+  // node arrays up to kAcceptCommitSmemBytes beside the staged slots
+  return cudaFuncSetAttribute(k_accept_commit<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kAcceptCommitSmemBytes));
+}
 
 bool accept_commit_fits(int32_t batch, int32_t nodes) {
   return batch >= 1 && batch <= kSmallGreedyBatch &&

@@ -38,6 +38,8 @@ cudaError_t device_info(DeviceInfo* info) {
     if (e != cudaSuccess) return e;
     e = sample_smem_setup();
     if (e != cudaSuccess) return e;
+    e = accept_smem_setup();
+    if (e != cudaSuccess) return e;
     if (d.stats_blocks_per_sm[0] < 1) d.stats_blocks_per_sm[0] = 1;
     if (d.stats_blocks_per_sm[1] < 1) d.stats_blocks_per_sm[1] = 1;
     cache[dev] = d;

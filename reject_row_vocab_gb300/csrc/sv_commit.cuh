@@ -62,8 +62,11 @@ __device__ __forceinline__ Tv block_exclusive_scan(Tv v, Tv* smem, Tv* total) {
 // of a block: commit_cu = exclusive
 // scan of num_out; for committed row k of request b, its KV slot and its
 // destination position seq_lens[b] + k.  Needs only the acceptance results.
+// s_slots / s_seq: copies of row_slots / seq_lens staged in shared memory by
+// the caller, or NULL to read them from global memory.
 template <bool NAMED>
-__device__ __forceinline__ void commit_block_t(const OutView& out, const CommitParams& cp) {
+__device__ __forceinline__ void commit_block_t(const OutView& out, const CommitParams& cp,
+                                               const int64_t* s_slots = nullptr, const int64_t* s_seq = nullptr) {
   __shared__ int64_t s_scan[kCommitThreads / 32 + 1];
   const int B = cp.batch, ML = cp.max_len;
   const int per = (B + kCommitThreads - 1) / kCommitThreads;
@@ -89,13 +92,14 @@ __device__ __forceinline__ void commit_block_t(const OutView& out, const CommitP
     const int32_t row = out.accept_rows[e];
     const int64_t base = out.commit_cu[b];
     if (k >= n) continue;
-    if (out.commit_src_slot && cp.row_slots) out.commit_src_slot[base + k] = cp.row_slots[row];
-    if (out.commit_dst_pos && cp.seq_lens) out.commit_dst_pos[base + k] = cp.seq_lens[b] + k;
+    if (out.commit_src_slot && cp.row_slots) out.commit_src_slot[base + k] = s_slots ? s_slots[row] : cp.row_slots[row];
+    if (out.commit_dst_pos && cp.seq_lens) out.commit_dst_pos[base + k] = (s_seq ? s_seq[b] : cp.seq_lens[b]) + k;
   }
 }
 
 __device__ __forceinline__ void commit_block(const OutView& out, const CommitParams& cp) { commit_block_t<false>(out, cp); }
-__device__ __forceinline__ void commit_block_named(const OutView& out, const CommitParams& cp) {
-  commit_block_t<true>(out, cp);
+__device__ __forceinline__ void commit_block_named(const OutView& out, const CommitParams& cp,
+                                                   const int64_t* s_slots = nullptr, const int64_t* s_seq = nullptr) {
+  commit_block_t<true>(out, cp, s_slots, s_seq);
 }
 }  // namespace sv

@@ -280,6 +280,7 @@ cudaError_t launch_accept_tree(const TreeParams& p, const OutView& out, const Ws
 constexpr int kSmallGreedyBatch = 32;
 constexpr int64_t kAcceptCommitSmemBytes = 48 * 1024;
 bool accept_commit_fits(int32_t batch, int32_t nodes);  // nodes <= 0: a chain
+cudaError_t accept_smem_setup();
 cudaError_t launch_accept_commit_chain(const ChainParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
                                        cudaStream_t stream);
 cudaError_t launch_accept_commit_tree(const TreeParams& p, const OutView& out, const CommitParams& cp, const Ws& ws,
