@@ -46,6 +46,12 @@ def test_status_strings_and_workspace_size(lib):
     big = lib.spec_verify_workspace_bytes(1024, 64, 151936, 16)
     assert 0 < small < big
     assert big % 256 == 0
+    # a sparse q's candidate lists are read in place: its workspace is the dense one, whatever num_cands is
+    lib.spec_verify_sparse_workspace_bytes.restype = ctypes.c_size_t
+    lib.spec_verify_sparse_workspace_bytes.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                                       ctypes.c_int32, ctypes.c_int32]
+    for k in (1, 16, 1024):
+        assert lib.spec_verify_sparse_workspace_bytes(1024, 64, 151936, 16, k) == big
 
 
 def _out_struct(addr=0x10000):

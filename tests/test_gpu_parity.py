@@ -185,6 +185,13 @@ def test_greedy_batch_sizes_around_the_single_cta_path(batch):
     check(w, use_lists=True)
 
 
+@pytest.mark.parametrize("batch,m", [(16, 63), (20, 63)])
+def test_single_cta_commit_with_slots_staged_or_read(batch, m):
+    """The one-CTA greedy path copies the KV slots of up to 1024 rows to shared memory before its wait (16 x 64
+    rows) and reads them from global memory beyond that (20 x 64 rows): the commit lists match the oracle."""
+    check(wl.greedy_chain(batch=batch, m=m, vocab=3001, dtype="bf16", p_match=0.93, seed=batch + m))
+
+
 def test_chain_and_tree_entry_points_agree():
     w = wl.greedy_chain(batch=20, m=7, vocab=3000, dtype="bf16", p_match=0.85, seed=5)
     L = 8
