@@ -39,7 +39,11 @@
 //     accept the first child with u < c/theta_acc or p(tok) >= theta_single.  A child whose
 //     token repeats an earlier sibling's is skipped (status bit 32).  If none is accepted,
 //     sample from p with the children's tokens zeroed; at a leaf, sample from p.
-//     PARITY UNPINNED for theta_single < 1 or theta_acc < 1 (a lossy rule no page fixes).
+//     Thresholds other than 1 make the rule lossy and no page fixes them; the reading is pinned
+//     by its special cases (theta_single = 0 takes the first child at every level and is
+//     inclusive at p = 0; no child passing stops at the root with the children excluded; a huge
+//     theta_acc leaves the first child at or above theta_single) and by the acceptance law
+//     min(1, c_i/theta_acc) - min(1, c_(i-1)/theta_acc) of child i.
 //   * a tree that fails validation is verified as its root alone (status bit 4).
 //   * a request whose row range is invalid commits nothing (status bit 8).
 //

@@ -174,6 +174,19 @@ def test_tree_small(mode, V, keep):
     check(w, use_lists=True)
 
 
+@pytest.mark.parametrize("th_single,th_acc", [(0.0, 1.0), (2.0, 1e30), (0.3, 0.7), (0.05, 0.5), (1.5, 0.25)])
+def test_target_only_thresholds(th_single, th_acc):
+    """Target-only walks with thresholds other than 1 (first child always; never a child; single-token and
+    cumulative acceptance mixed) match the oracle, with and without sibling lists."""
+    import dataclasses
+    w = wl.eagle2_tree(batch=10, topk=4, depth=4, keep=20, vocab=4099, mode="target_only_tree", noise_sigma=0.5,
+                       temperature=0.9, seed=int(th_single * 100 + th_acc * 10) % 1000 + 3)
+    w = dataclasses.replace(w, threshold_single=th_single, threshold_acc=th_acc)
+    check(w)
+    w.first_child, w.next_sibling = wl.sibling_lists(w.parents)
+    check(w, use_lists=True)
+
+
 @pytest.mark.parametrize("batch", [1, 32, 33, 70])
 def test_greedy_batch_sizes_around_the_single_cta_path(batch):
     """Greedy calls of at most 32 requests are accepted and committed by one CTA; larger ones by the acceptance

@@ -364,7 +364,7 @@ def test_chain_is_a_tree_special_case():
         assert np.array_equal(oc[k], ot[k]), k
 
 
-def _target_only_case(n, seed=9, th=1.0):
+def _target_only_case(n, seed=9, th=1.0, th_single=None, th_acc=None):
     """A fixed small tree, replicated n times with fresh uniforms."""
     rng = np.random.default_rng(seed)
     V, N = 7, 5
@@ -375,7 +375,7 @@ def _target_only_case(n, seed=9, th=1.0):
     lg = np.tile(base, (n, 1))
     w = tree_workload(lg, "f32", np.tile(tok, (n, 1)), np.tile(par, (n, 1)), T=np.full(n, T),
                       ua=wl.uniforms(rng, n * N), uf=wl.uniforms(rng, n), kind="target_only_tree",
-                      th_single=th, th_acc=th)
+                      th_single=th if th_single is None else th_single, th_acc=th if th_acc is None else th_acc)
     p = [softmax(base[i].astype(np.float64) / np.float64(np.float32(T))) for i in range(N)]
     return w, p, tok, par
 
@@ -431,6 +431,86 @@ def test_target_only_with_chain_tree_matches_rejection_of_p():
     assert chi_square_pvalue(np.bincount(o["out_tokens"][:, 0], minlength=V), p0) > 1e-4
     m = o["accept_len"] >= 1
     assert chi_square_pvalue(np.bincount(o["out_tokens"][m, 1], minlength=V), p1) > 1e-4
+
+
+# Thresholds other than 1 (a lossy rule; these pin the reading written in the
+# oracle's header through special cases and the law it implies, with p from
+# numpy, not through the oracle's own formula).
+
+
+def test_target_only_single_threshold_zero_walks_the_first_children():
+    """theta_single = 0: every child passes p >= theta_single, so the walk takes the first child at every level
+    (root -> node 1 -> node 3, a leaf) whatever the uniforms, and the last token is drawn from the leaf's row."""
+    n = 30000
+    w, p, tok, par = _target_only_case(n, th_single=0.0, th_acc=1.0)
+    o = oracle.verify_tree(w, "target_only", threads=4)
+    assert np.all(o["accept_len"] == 2)
+    assert np.all(o["out_tokens"][:, 0] == tok[1]) and np.all(o["out_tokens"][:, 1] == tok[3])
+    assert np.all(o["accept_rows"][:, :3] % 5 == [0, 1, 3])
+    assert chi_square_pvalue(np.bincount(o["out_tokens"][:, 2], minlength=w.vocab), p[3]) > 1e-4
+
+
+def test_target_only_single_threshold_is_inclusive():
+    """p(token) >= theta_single accepts: with theta_single = 0 a first child whose token has probability 0 under
+    the root's row (logit -inf) is still accepted."""
+    w, p, tok, par = _target_only_case(50, th_single=0.0, th_acc=1.0)
+    lg = w.logits.copy()
+    lg[0::5, tok[1]] = -np.inf  # every request's root row
+    w.logits = lg
+    o = oracle.verify_tree(w, "target_only")
+    assert np.all(o["accept_len"] >= 1) and np.all(o["accept_rows"][:, 1] % 5 == 1)
+
+
+def test_target_only_no_child_can_pass_stops_at_the_root():
+    """theta_acc huge and theta_single above 1: no child is ever accepted, so every request stops at the root and
+    draws from the root's p with the children's tokens removed."""
+    n = 30000
+    w, p, tok, par = _target_only_case(n, th_single=2.0, th_acc=1e30)
+    o = oracle.verify_tree(w, "target_only", threads=4)
+    assert np.all(o["accept_len"] == 0)
+    q = p[0].copy()
+    q[tok[[1, 2, 4]]] = 0.0
+    q /= q.sum()
+    assert chi_square_pvalue(np.bincount(o["out_tokens"][:, 0], minlength=w.vocab), q) > 1e-4
+
+
+def test_target_only_single_threshold_picks_the_first_child_above_it():
+    """theta_acc huge: only p(token) >= theta_single accepts, so the accepted child is the first one (in sibling
+    order) whose probability reaches the threshold, the same for every uniform."""
+    w1, p, tok, par = _target_only_case(1)
+    kids = [1, 2, 4]
+    pk = sorted(p[0][tok[k]] for k in kids)
+    for lo, hi in zip(pk[:-1], pk[1:]):
+        if hi - lo < 1e-3:
+            continue
+        th = 0.5 * (lo + hi)
+        w, _, _, _ = _target_only_case(200, th_single=th, th_acc=1e30)
+        o = oracle.verify_tree(w, "target_only")
+        first = next(k for k in kids if p[0][tok[k]] >= th)
+        assert np.all(o["accept_len"] >= 1) and np.all(o["accept_rows"][:, 1] % 5 == first)
+        if first == 1:  # node 1's only child (node 3) passes iff its probability under node 1's row reaches th
+            deeper = p[1][tok[3]] >= th
+            assert np.all((o["accept_len"] == 2) == deeper)
+
+
+def test_target_only_acceptance_threshold_law():
+    """theta_single above 1 and theta_acc < 1: at the root child i is accepted w.p.
+    min(1, c_i / theta_acc) - min(1, c_(i-1) / theta_acc), c_i the children's cumulative probability in sibling
+    order, and the walk stops there w.p. 1 - min(1, c_last / theta_acc)."""
+    n = 60000
+    th = 0.6
+    w, p, tok, par = _target_only_case(n, th_single=2.0, th_acc=th)
+    o = oracle.verify_tree(w, "target_only", threads=4)
+    kids = [1, 2, 4]
+    c = np.cumsum([p[0][tok[k]] for k in kids])
+    lo = np.minimum(1.0, np.concatenate([[0.0], c[:-1]]) / th)
+    hi = np.minimum(1.0, c / th)
+    for k, a, b in zip(kids, lo, hi):
+        pk = b - a
+        frac = np.mean((o["accept_len"] >= 1) & (o["accept_rows"][:, 1] % 5 == k))
+        assert abs(frac - pk) < 5 * np.sqrt(max(pk * (1 - pk), 1e-12) / n) + 1e-9, (k, frac, pk)
+    stop = 1.0 - hi[-1]
+    assert abs(np.mean(o["accept_len"] == 0) - stop) < 5 * np.sqrt(max(stop * (1 - stop), 1e-12) / n) + 1e-9
 
 
 # ---------------------------------------------------------------------------
