@@ -1,0 +1,71 @@
+"""The oracle's pins fail on planted mistakes.
+
+Each case copies oracle/oracle.cpp, plants one plausible mistake in the copy (a
+swapped acceptance test, a dropped temperature, an unclamped residual, a wrong
+tie-break, a misread threshold rule, ...), builds it with the host compiler into
+a temporary directory and runs the pin tests against it in a child process: at
+least one pin must fail there.  The oracle itself is never modified.
+"""
+import os
+import subprocess
+import sys
+import textwrap
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.cpp")
+PINS = ["tests/test_oracle_pins.py", "tests/test_oracle_gaps.py"]
+
+# name -> [(text in the oracle, planted replacement), ...]; each text occurs exactly once
+MUTATIONS = {
+    "acceptance test swapped, u*p < q": [("return u * q < p;", "return u * p < q;")],
+    "argmax ties go to the highest index": [("if (l > r.M) {", "if (l >= r.M) {")],
+    "temperature dropped from the softmax": [
+        ("Z += std::exp((l - r.M) / T);", "Z += std::exp(l - r.M);"),
+        ("return std::exp((l - r.M) / r.T) / r.Z;", "return std::exp(l - r.M) / r.Z;"),
+    ],
+    "residual taken as q - p": [
+        ("w[v] = std::max(0.0, p[v] - static_cast<double>(q[v]));",
+         "w[v] = std::max(0.0, static_cast<double>(q[v]) - p[v]);"),
+    ],
+    "residual not clamped at 0": [
+        ("w[v] = std::max(0.0, p[v] - static_cast<double>(q[v]));", "w[v] = p[v] - static_cast<double>(q[v]);"),
+    ],
+    "inverse CDF target not scaled by the total": [("double t = u * S;", "double t = u;")],
+    "greedy tree accepts a child that is not the argmax": [("if (tok[k] == st.argmax) {", "if (tok[k] != st.argmax) {")],
+    "theta_acc multiplies the cumulative mass": [
+        ("if (u < c / a.th_acc || pk >= a.th_single) {", "if (u < c * a.th_acc || pk >= a.th_single) {"),
+    ],
+    "theta_single compared strictly": [
+        ("if (u < c / a.th_acc || pk >= a.th_single) {", "if (u < c / a.th_acc || pk > a.th_single) {"),
+    ],
+    "target-only stop draw keeps the children": [("for (int32_t t : seen) w[t] = 0.0;", "for (int32_t t : seen) (void)t;")],
+    "cumulative mass taken before the child": [
+        ("if (u < c / a.th_acc || pk >= a.th_single) {", "if (u < (c - pk) / a.th_acc || pk >= a.th_single) {"),
+    ],
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_fail_on_a_planted_mistake(name, tmp_path):
+    src = open(SRC).read()
+    for old, new in MUTATIONS[name]:
+        assert src.count(old) == 1, (name, old)
+        src = src.replace(old, new)
+    cpp = tmp_path / "oracle_planted.cpp"
+    cpp.write_text(src)
+    lib = str(tmp_path / "liboracle_planted.so")
+    subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", str(cpp), "-o", lib])
+    code = textwrap.dedent("""
+        import sys
+        sys.path.insert(0, %r)
+        import oracle
+        oracle._LIB = %r
+        oracle.build = lambda force=False: %r
+        import pytest
+        sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", *%r]))
+    """) % (ROOT, lib, lib, PINS)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    # exit status 1: tests ran and one failed (0 would mean every pin passed; anything else a crash or an error)
+    assert r.returncode == 1, (name, r.returncode, r.stdout[-3000:], r.stderr[-2000:])
