@@ -49,6 +49,9 @@ def test_budget_edge_cases():
     assert dspark.budget([0.9, float("nan"), 0.01], 1, sps, eps=0.05) == 1  # NaN and sub-eps scores dropped
     # a flat speed table takes every positive score
     assert dspark.budget([0.3, 0.2, 0.1], 2, [1.0] * 10) == 3
+    # equal predicted throughput keeps the smaller K: N(K) * SPS(1 + K) = 1*6 = 2*3 = 3*2 exactly
+    assert dspark.budget([1.0, 1.0], 1, [0.0, 6.0, 3.0, 2.0]) == 0
+    assert dspark.budget([1.0, 1.0], 1, [0.0, 5.0, 3.0, 2.0]) == 1  # K = 1 and K = 2 tie above K = 0
 
 
 def test_monotone_rows_get_prefixes_and_the_budget_is_spent():
@@ -105,6 +108,9 @@ def test_library_budget_matches_the_page_and_the_oracle():
         # the oracle in fp64 over the same fp32 inputs
         want = dspark.budget(hist.astype(np.float64).tolist(), R, sps.astype(np.float64).tolist(), eps)
         assert sv.dspark_budget(hist, R, sps, eps) == want
+    # exact ties keep the smaller K in the library too
+    assert sv.dspark_budget(np.array([1.0, 1.0], np.float32), 1, np.array([0.0, 6.0, 3.0, 2.0], np.float32)) == 0
+    assert sv.dspark_budget(np.array([1.0, 1.0], np.float32), 1, np.array([0.0, 5.0, 3.0, 2.0], np.float32)) == 1
 
 
 def test_library_scheduler_host_validation():

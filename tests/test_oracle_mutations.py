@@ -1,12 +1,14 @@
 """The oracle's pins fail on planted mistakes.
 
-Each case copies oracle/oracle.cpp, plants one plausible mistake in the copy (a
+Each case copies the oracle, plants one plausible mistake in the copy (a
 swapped acceptance test, a dropped temperature, an unclamped residual, a wrong
-tie-break, a misread threshold rule, ...), builds it with the host compiler into
-a temporary directory and runs the pin tests against it in a child process: at
-least one pin must fail there.  The oracle itself is never modified.
+tie-break, a misread threshold rule, a wrong scheduling order, ...), builds it
+with the host compiler into a temporary directory and runs the pin tests
+against it in a child process: at least one pin must fail there.  The oracle
+itself is never modified.
 """
 import os
+import shutil
 import subprocess
 import sys
 import textwrap
@@ -68,4 +70,54 @@ def test_pins_fail_on_a_planted_mistake(name, tmp_path):
     """) % (ROOT, lib, lib, PINS)
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
     # exit status 1: tests ran and one failed (0 would mean every pin passed; anything else a crash or an error)
+    assert r.returncode == 1, (name, r.returncode, r.stdout[-3000:], r.stderr[-2000:])
+
+
+# The Python oracles: name -> (file under oracle/, [(text, planted replacement)], pin files)
+PY_MUTATIONS = {
+    "DSpark budget sorts the survival scores ascending": (
+        "dspark.py",
+        [("reverse=True)\n    best_k, best = 0, -math.inf", "reverse=False)\n    best_k, best = 0, -math.inf")],
+        ["tests/test_dspark_oracle.py"]),
+    "DSpark budget ties keep the larger K": (
+        "dspark.py", [("        if score > best:", "        if score >= best:")], ["tests/test_dspark_oracle.py"]),
+    "DSpark top-K orders ties by request before position": (
+        "dspark.py", [("cands.append((-key, j, r, s))", "cands.append((-key, r, j, s))")],
+        ["tests/test_dspark_oracle.py"]),
+    "sample-then-match accepts a mismatching draft": (
+        "match.py", [("            if d != t:", "            if d == t:")], ["tests/test_match_oracle.py"]),
+    "tree depth from the previous index instead of the parent": (
+        "tree_build.py", [("depth[i] = depth[parents[i]] + 1", "depth[i] = depth[i - 1] + 1")],
+        ["tests/test_tree_build_oracle.py"]),
+    "next sibling is the last one instead of the next": (
+        "tree_build.py", [("later[0] if later else -1", "later[-1] if later else -1")],
+        ["tests/test_tree_build_oracle.py"]),
+    "parity rule exempts every acceptance test": (
+        "parity.py", [("close = np.nonzero(test_gap[b] < tol)[0]", "close = np.nonzero(test_gap[b] < 1.0)[0]")],
+        ["tests/test_parity_rule.py"]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_python_oracle_pins_fail_on_a_planted_mistake(name, tmp_path):
+    fname, edits, pins = PY_MUTATIONS[name]
+    pkg = tmp_path / "oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), pkg,
+                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    path = pkg / fname
+    src = path.read_text()
+    for old, new in edits:
+        assert src.count(old) == 1, (name, old)
+        src = src.replace(old, new)
+    path.write_text(src)
+    code = textwrap.dedent("""
+        import sys
+        sys.path.insert(0, %r)
+        sys.path.insert(0, %r)
+        import oracle, oracle.dspark, oracle.match, oracle.tree_build, oracle.parity
+        assert oracle.__file__.startswith(%r), oracle.__file__
+        import pytest
+        sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", *%r]))
+    """) % (ROOT, str(tmp_path), str(tmp_path), pins)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 1, (name, r.returncode, r.stdout[-3000:], r.stderr[-2000:])
