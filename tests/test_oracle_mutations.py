@@ -46,6 +46,18 @@ MUTATIONS = {
     "cumulative mass taken before the child": [
         ("if (u < c / a.th_acc || pk >= a.th_single) {", "if (u < (c - pk) / a.th_acc || pk >= a.th_single) {"),
     ],
+    "final token drawn from the row before the stop": [
+        ("const int64_t s = start + j;", "const int64_t s = start + (j > 0 ? j - 1 : 0);"),
+    ],
+    "acceptance gap measured as |u - q/p|": [
+        ("std::fabs(u - p / qd)", "std::fabs(u - qd / p)"),
+    ],
+    "committed rows of a request written in reverse": [
+        ("int64_t dst = o.commit_cu[b] + k;", "int64_t dst = o.commit_cu[b + 1] - 1 - k;"),
+    ],
+    "destination position one past the committed offset": [
+        ("o.commit_dst_pos[dst] = seq_lens[b] + k;", "o.commit_dst_pos[dst] = seq_lens[b] + k + 1;"),
+    ],
 }
 
 
@@ -92,6 +104,9 @@ PY_MUTATIONS = {
     "next sibling is the last one instead of the next": (
         "tree_build.py", [("later[0] if later else -1", "later[-1] if later else -1")],
         ["tests/test_tree_build_oracle.py"]),
+    "sparse q keeps the last of repeated ids instead of their sum": (
+        "__init__.py", [("np.add.at(q, (rr[ok], ids[ok]), pr[ok])", "q[rr[ok], ids[ok]] = pr[ok]")],
+        ["tests/test_sparse_oracle.py"]),
     "parity rule exempts every acceptance test": (
         "parity.py", [("close = np.nonzero(test_gap[b] < tol)[0]", "close = np.nonzero(test_gap[b] < 1.0)[0]")],
         ["tests/test_parity_rule.py"]),
