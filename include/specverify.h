@@ -297,11 +297,17 @@ sv_status_t spec_verify_set_hand_off_limit_ns(uint64_t ns);
 
 /*
  * Row statistics on their own (the single pass every entry point starts
- * with): for each of `rows` rows, the maximum M (float), the lowest argmax
- * (-1 for an all -inf row), Z = sum_v exp((l_v - M)/T) with T = row_temp[row]
- * (0 when row_temp is NULL or the row is greedy), p at probe[row] (when
- * probe and out_p are given), and SV_DEV_NONFINITE in row_flags.
- * out_z is double.  All outputs [rows]; out_p / probe / row_temp may be NULL.
+ * with; [E2D] §1.2 and §6.2: the target distribution of a row is
+ * softmax(l / T), and a greedy row takes its argmax): for each of `rows`
+ * rows, the maximum M (float), the lowest argmax (-1 for an all -inf row),
+ * Z = sum_v exp((l_v - M)/T) with T = row_temp[row] (0 when row_temp is NULL
+ * or the row is greedy), p at probe[row] (when probe and out_p are given),
+ * and SV_DEV_NONFINITE in row_flags.  out_z is double.  All outputs [rows],
+ * device, caller-owned; out_p / probe / row_temp may be NULL.  ws: at least
+ * spec_verify_workspace_bytes(rows, 1, vocab, 1) bytes (same rules as every
+ * workspace).  Argument errors (SV_ERR_NULL_ARG for a missing logits,
+ * out_max, out_argmax or out_z; the logits checks of every entry point)
+ * return before anything is enqueued.
  */
 sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t ld, int64_t rows, int32_t vocab,
                                   const float* row_temp, const int32_t* probe, float* out_max,
@@ -337,6 +343,15 @@ sv_status_t spec_verify_row_stats(const void* logits, sv_dtype_t dtype, int64_t 
  * min_len < 1, max_len < min_len, R * D > 2^30; SV_ERR_WORKSPACE_TOO_SMALL)
  * return before anything is enqueued.
  */
+size_t spec_verify_dspark_workspace_bytes(int32_t num_requests);
+
+sv_status_t spec_verify_dspark_budget(const float* hist_survival, int64_t n, int32_t num_requests, const float* sps,
+                                      int32_t sps_len, float eps, int32_t* k_star);
+
+sv_status_t spec_verify_dspark_verify_lens(const float* survival, int32_t num_requests, int32_t num_drafts,
+                                           int64_t ld, int32_t budget, int32_t min_len, int32_t max_len, float eps,
+                                           int32_t* verify_lens, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /*
  * Tree-verify inputs from parent lists ([E2D] §2.4: a flattened tree where each
  * node sees the committed history, its ancestors and itself, with position ids
@@ -362,15 +377,6 @@ sv_status_t spec_verify_build_tree(const int32_t* parents, const int64_t* seq_le
                                    int64_t* positions, uint8_t* mask, int32_t* retrieve_index,
                                    int32_t* first_child, int32_t* next_sibling, uint32_t* status,
                                    cudaStream_t stream);
-
-size_t spec_verify_dspark_workspace_bytes(int32_t num_requests);
-
-sv_status_t spec_verify_dspark_budget(const float* hist_survival, int64_t n, int32_t num_requests, const float* sps,
-                                      int32_t sps_len, float eps, int32_t* k_star);
-
-sv_status_t spec_verify_dspark_verify_lens(const float* survival, int32_t num_requests, int32_t num_drafts,
-                                           int64_t ld, int32_t budget, int32_t min_len, int32_t max_len, float eps,
-                                           int32_t* verify_lens, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
