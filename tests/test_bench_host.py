@@ -69,7 +69,26 @@ def test_aux_modes_inputs_and_reference_arm(capsys):
         bench.main(["--impl", "reference", "--kernel", kind, "--steps", "2", "--warmup", "1"])
         line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
         assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
-        assert line["metric"] == bench.AUX[kind]["metric"]
+        assert line["metric"] == bench.AUX[kind]["metric"] and line["warmup"] == 3
+
+
+def test_step_reference_arm_line(capsys):
+    """The reference arm of the verify step (the oracle on the host cores) prints one line with the contract's keys:
+    its own value in cpu_baseline and e2e, no host-device bytes, the workload named in config."""
+    import bench
+    bench.main(["--impl", "reference", "--config", "1", "--steps", "2", "--warmup", "1"])
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
+    assert line["warmup"] == 3  # the bench runs at least three warm-up steps and reports what it ran
+    assert line["config"]["workload"] == "c1_greedy_chain" and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e = line["e2e"]
+    assert e["value"] == line["value"] and e["unit"] == line["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
 
 
 def test_stats_event_slots():
