@@ -55,6 +55,12 @@ MUTATIONS = {
     "committed rows of a request written in reverse": [
         ("int64_t dst = o.commit_cu[b] + k;", "int64_t dst = o.commit_cu[b + 1] - 1 - k;"),
     ],
+    "row statistics report p at the argmax instead of the probe": [
+        ("pv = prob(st, lg.at(r, probe[r]));", "pv = prob(st, lg.at(r, st.argmax));"),
+    ],
+    "row statistics flag nothing for NaN or +inf": [
+        ("out_flags[r] = st.nonfinite ? kNonFinite : 0u;", "out_flags[r] = 0u;"),
+    ],
     "destination position one past the committed offset": [
         ("o.commit_dst_pos[dst] = seq_lens[b] + k;", "o.commit_dst_pos[dst] = seq_lens[b] + k + 1;"),
     ],

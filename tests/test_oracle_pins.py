@@ -166,6 +166,24 @@ def test_row_stats_match_library_routines():
     assert s["argmax"][2] == 17
 
 
+def test_row_stats_nonfinite_entries():
+    """NaN and +inf are left out of the maximum, the argmax and Z and flag their row (bit 2); -inf is an ordinary
+    entry of weight 0; a row of -inf only has no argmax.  Checked against numpy over the remaining entries."""
+    x = np.array([[0.5, np.nan, 2.0, -1.0],
+                  [np.inf, 1.0, 3.0, 3.0],
+                  [-np.inf, -np.inf, -np.inf, -np.inf],
+                  [0.0, -np.inf, 1.0, 0.25]], np.float32)
+    T = np.full(4, 0.7, np.float32)
+    s = oracle.row_stats(x, "f32", row_temp=T)
+    assert list(s["flags"]) == [2, 2, 0, 0]
+    assert list(s["argmax"]) == [2, 2, -1, 2]
+    for r in (0, 1, 3):
+        keep = np.isfinite(x[r]) | (x[r] == -np.inf)
+        v = x[r][keep].astype(np.float64)
+        assert s["max"][r] == v.max()
+        assert abs(s["z"][r] - np.exp((v - v.max()) / float(T[r])).sum()) < 1e-12 * s["z"][r]
+
+
 # ---------------------------------------------------------------------------
 # Rejection test, residual, sampler
 # ---------------------------------------------------------------------------
