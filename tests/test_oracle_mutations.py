@@ -61,6 +61,13 @@ MUTATIONS = {
     "row statistics flag nothing for NaN or +inf": [
         ("out_flags[r] = st.nonfinite ? kNonFinite : 0u;", "out_flags[r] = 0u;"),
     ],
+    "children found from the node after the current one only": [
+        ("for (int32_t i = cur + 1; i < a.N; ++i)\n      if (par[i] == cur) kids.push_back(i);",
+         "for (int32_t i = cur + 2; i < a.N; ++i)\n      if (par[i] == cur) kids.push_back(i);"),
+    ],
+    "tree validation accepts a parent that is not before its node": [
+        ("if (par[i] < 0 || par[i] >= i) return false;", "if (par[i] < 0 || par[i] >= a.N) return false;"),
+    ],
     "destination position one past the committed offset": [
         ("o.commit_dst_pos[dst] = seq_lens[b] + k;", "o.commit_dst_pos[dst] = seq_lens[b] + k + 1;"),
     ],
@@ -113,6 +120,17 @@ PY_MUTATIONS = {
     "sparse q keeps the last of repeated ids instead of their sum": (
         "__init__.py", [("np.add.at(q, (rr[ok], ids[ok]), pr[ok])", "q[rr[ok], ids[ok]] = pr[ok]")],
         ["tests/test_sparse_oracle.py"]),
+    "DSpark verify lengths leave out the anchor row": (
+        "dspark.py", [("return [min(max(1 + e, min_len), max_len) for e in extra]",
+                       "return [min(max(e, min_len), max_len) for e in extra]")],
+        ["tests/test_dspark_oracle.py"]),
+    "sparse q flags padding ids as out of range": (
+        "__init__.py", [("bad = np.any((ids != -1) & ~ok, axis=1)", "bad = np.any(~ok, axis=1)")],
+        ["tests/test_sparse_oracle.py"]),
+    "parity rule lets a close final draw exempt the whole request": (
+        "parity.py", [("            for k in (\"accept_len\", \"num_out\", \"accept_rows\", \"status\"):",
+                       "            for k in ():")],
+        ["tests/test_parity_rule.py"]),
     "parity rule exempts every acceptance test": (
         "parity.py", [("close = np.nonzero(test_gap[b] < tol)[0]", "close = np.nonzero(test_gap[b] < 1.0)[0]")],
         ["tests/test_parity_rule.py"]),

@@ -71,6 +71,10 @@ def test_close_draw_exempts_only_the_drawn_token():
     g["accept_len"][b] = max(0, r - 1) if r else 1  # the accepted length is still certain
     assert compare(w2, g, o2, check=False)["mismatch"] >= 1
     g = copy.deepcopy(o2)
+    g["bonus"][b] = g["out_tokens"][b, r] = other
+    g["status"][b] |= 16  # a valid path with a wrong status bit: the status stays exact too
+    assert compare(w2, g, o2, check=False)["mismatch"] >= 1
+    g = copy.deepcopy(o2)
     g["bonus"][b] = g["out_tokens"][b, r] = w.vocab  # the drawn token must be a valid id
     assert compare(w2, g, o2, check=False)["mismatch"] >= 1
 
