@@ -68,6 +68,12 @@ MUTATIONS = {
     "tree validation accepts a parent that is not before its node": [
         ("if (par[i] < 0 || par[i] >= i) return false;", "if (par[i] < 0 || par[i] >= a.N) return false;"),
     ],
+    "chain residual fallback to p not flagged": [
+        ("  if (v < 0) {\n    rr.status |= kResidualEmpty;\n", "  if (v < 0) {\n"),
+    ],
+    "repeated sibling token not flagged": [("          rr.status |= kDupSibling;\n", "")],
+    "invalid tree not flagged": [("  if (!ok_tree) rr.status |= kBadTree;", "  (void)ok_tree;")],
+    "invalid row range not flagged": [("    rr.status |= kBadLayout;", "")],
     "destination position one past the committed offset": [
         ("o.commit_dst_pos[dst] = seq_lens[b] + k;", "o.commit_dst_pos[dst] = seq_lens[b] + k + 1;"),
     ],

@@ -531,6 +531,34 @@ def test_target_only_acceptance_threshold_law():
     assert abs(np.mean(o["accept_len"] == 0) - stop) < 5 * np.sqrt(max(stop * (1 - stop), 1e-12) / n) + 1e-9
 
 
+def test_empty_residual_falls_back_to_p_and_sets_bit_16():
+    """q >= p everywhere on a rejected row leaves [p - q]+ empty: the final token is drawn from p itself (inverse
+    CDF over a uniform p of four ids, u = 0.6 -> id 2) and the request reports status bit 16."""
+    lg = np.zeros((2, 4), np.float32)                 # p = 1/4 on both rows
+    q = np.full((2, 4), 0.5, np.float32)              # not normalised: q(v) > p(v) for every v
+    w = chain_workload(lg, "f32", [0, 2], np.array([0, 0], np.int32), q=q, T=np.ones(1),
+                       ua=np.array([0.9, 0.5], np.float32), uf=np.array([0.6], np.float32))
+    o = oracle.verify_chain(w)
+    assert o["accept_len"][0] == 0                    # 0.9 * 0.5 >= 0.25: rejected
+    assert int(o["status"][0]) & 16
+    assert o["bonus"][0] == 2
+
+
+def test_repeated_sibling_token_is_skipped_and_flagged():
+    """A target-only walk counts a repeated sibling token once and flags it (bit 32): with p = 1/5 everywhere,
+    children tokens (3, 3, 1) and u = 0.5 at the root, the cumulative mass reaches 0.2 then 0.4 (not 0.6), no child
+    is accepted, and the stop draw over p without ids 3 and 1 takes id 2 for u_final = 0.5."""
+    lg = np.zeros((4, 5), np.float32)
+    tok = np.array([[0, 3, 3, 1]], np.int32)
+    par = np.array([[-1, 0, 0, 0]], np.int32)
+    w = tree_workload(lg, "f32", tok, par, T=np.ones(1), ua=np.array([0.5, 0.5, 0.5, 0.5], np.float32),
+                      uf=np.array([0.5], np.float32), kind="target_only_tree")
+    o = oracle.verify_tree(w, "target_only")
+    assert int(o["status"][0]) & 32
+    assert o["accept_len"][0] == 0
+    assert o["bonus"][0] == 2
+
+
 # ---------------------------------------------------------------------------
 # Degenerate inputs
 # ---------------------------------------------------------------------------
