@@ -80,30 +80,6 @@ MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_pins_fail_on_a_planted_mistake(name, tmp_path):
-    src = open(SRC).read()
-    for old, new in MUTATIONS[name]:
-        assert src.count(old) == 1, (name, old)
-        src = src.replace(old, new)
-    cpp = tmp_path / "oracle_planted.cpp"
-    cpp.write_text(src)
-    lib = str(tmp_path / "liboracle_planted.so")
-    subprocess.check_call(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", str(cpp), "-o", lib])
-    code = textwrap.dedent("""
-        import sys
-        sys.path.insert(0, %r)
-        import oracle
-        oracle._LIB = %r
-        oracle.build = lambda force=False: %r
-        import pytest
-        sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", *%r]))
-    """) % (ROOT, lib, lib, PINS)
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
-    # exit status 1: tests ran and one failed (0 would mean every pin passed; anything else a crash or an error)
-    assert r.returncode == 1, (name, r.returncode, r.stdout[-3000:], r.stderr[-2000:])
-
-
 # The Python oracles: name -> (file under oracle/, [(text, planted replacement)], pin files)
 PY_MUTATIONS = {
     "DSpark budget sorts the survival scores ascending": (
@@ -143,26 +119,82 @@ PY_MUTATIONS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
-def test_python_oracle_pins_fail_on_a_planted_mistake(name, tmp_path):
+
+
+def _planted_source(name):
+    src = open(SRC).read()
+    for old, new in MUTATIONS[name]:
+        assert src.count(old) == 1, (name, old)
+        src = src.replace(old, new)
+    return src
+
+
+def _run_pins(sys_path, lib, pins):
+    """Run the pin files in a child process with `sys_path` first on its path (and, for a planted oracle.cpp,
+    its library in place of the oracle's own).  Returns (exit status, output tail)."""
+    setup = "oracle._LIB = %r\noracle.build = lambda force=False: %r\n" % (lib, lib) if lib else ""
+    code = textwrap.dedent("""
+        import sys
+        for p in %r:
+            sys.path.insert(0, p)
+        import oracle, oracle.dspark, oracle.match, oracle.tree_build, oracle.parity
+    """) % (sys_path,) + setup + textwrap.dedent("""
+        import pytest
+        sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", *%r]))
+    """) % (pins,)
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    return r.returncode, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def _cpp_case(name, d):
+    cpp = d / "oracle_planted.cpp"
+    cpp.write_text(_planted_source(name))
+    lib = str(d / "liboracle_planted.so")
+    r = subprocess.run(["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread", str(cpp), "-o", lib],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        return -1000, r.stderr[-2000:]
+    return _run_pins([ROOT], lib, PINS)
+
+
+def _py_case(name, d):
     fname, edits, pins = PY_MUTATIONS[name]
-    pkg = tmp_path / "oracle"
-    shutil.copytree(os.path.join(ROOT, "oracle"), pkg,
-                    ignore=shutil.ignore_patterns("*.so", "*.tmp*", "__pycache__"))
+    pkg = d / "oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), pkg, ignore=shutil.ignore_patterns("*.tmp*", "__pycache__"))
     path = pkg / fname
     src = path.read_text()
     for old, new in edits:
         assert src.count(old) == 1, (name, old)
         src = src.replace(old, new)
     path.write_text(src)
-    code = textwrap.dedent("""
-        import sys
-        sys.path.insert(0, %r)
-        sys.path.insert(0, %r)
-        import oracle, oracle.dspark, oracle.match, oracle.tree_build, oracle.parity
-        assert oracle.__file__.startswith(%r), oracle.__file__
-        import pytest
-        sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", *%r]))
-    """) % (ROOT, str(tmp_path), str(tmp_path), pins)
-    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 1, (name, r.returncode, r.stdout[-3000:], r.stderr[-2000:])
+    return _run_pins([ROOT, str(d)], None, pins)
+
+
+@pytest.fixture(scope="module")
+def planted(tmp_path_factory):
+    """Every planted case, built and run against the pins concurrently: (kind, name) -> (exit status, output)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.build()  # the Python cases copy the oracle with its library already built
+    cases = [("cpp", n) for n in sorted(MUTATIONS)] + [("py", n) for n in sorted(PY_MUTATIONS)]
+
+    def run(case):
+        kind, name = case
+        d = tmp_path_factory.mktemp("planted")
+        return (_cpp_case if kind == "cpp" else _py_case)(name, d)
+
+    with ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+        return dict(zip(cases, ex.map(run, cases)))
+
+
+# exit status 1: the pins ran and one failed (0 would mean every pin passed; anything else a crash or an error)
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_fail_on_a_planted_mistake(name, planted):
+    rc, out = planted[("cpp", name)]
+    assert rc == 1, (name, rc, out)
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_python_oracle_pins_fail_on_a_planted_mistake(name, planted):
+    rc, out = planted[("py", name)]
+    assert rc == 1, (name, rc, out)
