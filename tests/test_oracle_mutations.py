@@ -74,6 +74,32 @@ MUTATIONS = {
     "repeated sibling token not flagged": [("          rr.status |= kDupSibling;\n", "")],
     "invalid tree not flagged": [("  if (!ok_tree) rr.status |= kBadTree;", "  (void)ok_tree;")],
     "invalid row range not flagged": [("    rr.status |= kBadLayout;", "")],
+    "greedy chain accepts every draft": [("      ok = (st.argmax == d);", "      ok = true;")],
+    "chain draft outside the vocabulary not flagged": [
+        ("    if (d < 0 || d >= a.lg.vocab) {\n      rr.status |= kTokenRange;\n",
+         "    if (d < 0 || d >= a.lg.vocab) {\n"),
+    ],
+    "chain tested rows with NaN or +inf not flagged": [
+        ("    RowDist st = row_dist(a.lg, row, T);\n    if (st.nonfinite) rr.status |= kNonFinite;\n    if (st.argmax < 0) {\n      how = kUnusable;",
+         "    RowDist st = row_dist(a.lg, row, T);\n    if (st.argmax < 0) {\n      how = kUnusable;"),
+    ],
+    "greedy chain bonus from the first row": [
+        ("  if (greedy) {\n    rr.bonus = static_cast<int32_t>(st.argmax);\n    return rr;",
+         "  if (greedy) {\n    rr.bonus = static_cast<int32_t>(row_dist(a.lg, start, 0.0).argmax);\n    return rr;"),
+    ],
+    "greedy tree stop token is a child's token": [
+        ("      if (next < 0) {\n        rr.bonus = static_cast<int32_t>(st.argmax);",
+         "      if (next < 0) {\n        rr.bonus = kids.empty() ? static_cast<int32_t>(st.argmax) : tok[kids[0]];"),
+    ],
+    "commit offsets count the accepted drafts only": [
+        ("o.commit_cu[b + 1] = o.commit_cu[b] + o.num_out[b];", "o.commit_cu[b + 1] = o.commit_cu[b] + o.num_out[b] - 1;"),
+    ],
+    "draw gap not normalised by the total weight": [
+        ("const double lower = prev > 0.0 ? (t - prev) / S : kInf;", "const double lower = prev > 0.0 ? (t - prev) : kInf;"),
+    ],
+    "target-only gap ignores the single-token threshold": [
+        ("std::min(std::fabs(u - c / a.th_acc), std::fabs(pk - a.th_single))", "std::fabs(u - c / a.th_acc)"),
+    ],
     "destination position one past the committed offset": [
         ("o.commit_dst_pos[dst] = seq_lens[b] + k;", "o.commit_dst_pos[dst] = seq_lens[b] + k + 1;"),
     ],

@@ -559,6 +559,30 @@ def test_repeated_sibling_token_is_skipped_and_flagged():
     assert o["bonus"][0] == 2
 
 
+def test_nan_in_a_tested_row_is_flagged_and_verification_goes_on():
+    """A NaN in a tested row sets status bit 2 and is left out of that row's argmax; the request still accepts the
+    row's argmax draft and goes on to its bonus."""
+    lg = np.zeros((3, 6), np.float32)
+    lg[0, 2], lg[0, 4] = 1.0, np.nan
+    lg[1, 1] = 1.0
+    lg[2, 5] = 1.0
+    w = chain_workload(lg, "f32", [0, 3], np.array([0, 2, 1], np.int32))
+    o = oracle.verify_chain(w, greedy_all=True)
+    assert o["accept_len"][0] == 2 and o["bonus"][0] == 5
+    assert int(o["status"][0]) == 2
+
+
+def test_target_only_gap_includes_the_single_threshold():
+    """With theta_acc huge the cumulative test never decides; when a child's probability sits 1e-9 below
+    theta_single the step's gap is that distance, not the uniform's."""
+    w, p, tok, par = _target_only_case(1)
+    p1 = float(p[0][tok[1]])
+    w2, _, _, _ = _target_only_case(1, th_single=p1 + 1e-9, th_acc=1e30)
+    o = oracle.verify_tree(w2, "target_only")
+    assert o["test_gap"][0, 0] < 1e-8
+    assert o["min_gap"][0] < 1e-8
+
+
 # ---------------------------------------------------------------------------
 # Degenerate inputs
 # ---------------------------------------------------------------------------
