@@ -119,6 +119,17 @@ PY_MUTATIONS = {
         ["tests/test_dspark_oracle.py"]),
     "sample-then-match accepts a mismatching draft": (
         "match.py", [("            if d != t:", "            if d == t:")], ["tests/test_match_oracle.py"]),
+    "sample-then-match draws every row with the first row's uniform": (
+        "match.py", [("t, g = oracle.sample_index(p, float(w.u_accept[row]))",
+                      "t, g = oracle.sample_index(p, float(w.u_accept[start]))")],
+        ["tests/test_match_oracle.py"]),
+    "sample-then-match emits the draft instead of its own draw at a mismatch": (
+        "match.py", [("            if d != t:\n                s, tok = j, int(t)",
+                      "            if d != t:\n                s, tok = j, d")],
+        ["tests/test_match_oracle.py"]),
+    "sample-then-match draws from the argmax row at temperature 1": (
+        "match.py", [("p = oracle.row_probs(w.logits, w.dtype, row, T)", "p = oracle.row_probs(w.logits, w.dtype, row, 1.0)")],
+        ["tests/test_match_oracle.py"]),
     "tree depth from the previous index instead of the parent": (
         "tree_build.py", [("depth[i] = depth[parents[i]] + 1", "depth[i] = depth[i - 1] + 1")],
         ["tests/test_tree_build_oracle.py"]),
