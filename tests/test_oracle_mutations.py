@@ -150,6 +150,12 @@ PY_MUTATIONS = {
         "parity.py", [("            for k in (\"accept_len\", \"num_out\", \"accept_rows\", \"status\"):",
                        "            for k in ():")],
         ["tests/test_parity_rule.py"]),
+    "parity rule lets a close test exempt the prefix before it": (
+        "parity.py", [("            k0 = int(close[0])", "            k0 = 0")], ["tests/test_parity_rule.py"]),
+    "parity rule skips the validity check of a flagged request": (
+        "parity.py", [("        for msg in _path_valid(w, b, g):", "        for msg in []:")], ["tests/test_parity_rule.py"]),
+    "parity rule compares no commit lists once a request is flagged": (
+        "parity.py", [("        bad.extend(_commit_lists_ok(w, g))", "        pass")], ["tests/test_parity_rule.py"]),
     "parity rule exempts every acceptance test": (
         "parity.py", [("close = np.nonzero(test_gap[b] < tol)[0]", "close = np.nonzero(test_gap[b] < 1.0)[0]")],
         ["tests/test_parity_rule.py"]),

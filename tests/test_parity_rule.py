@@ -33,6 +33,15 @@ def _edge_uniform(w, o, b):
     return float(cdf[v]) + 1e-8
 
 
+def _recommit(w, g):
+    """Commit offsets and lists made consistent with g's committed rows."""
+    g["commit_cu"] = np.concatenate([[0], np.cumsum(g["num_out"])]).astype(np.int32)
+    n = int(g["commit_cu"][-1])
+    rows = np.concatenate([g["accept_rows"][i, :g["num_out"][i]] for i in range(w.batch)])
+    g["commit_src_slot"][:n] = w.row_slots[rows]
+    g["commit_dst_pos"][:n] = np.concatenate([w.seq_lens[i] + np.arange(g["num_out"][i]) for i in range(w.batch)])
+
+
 def test_identical_outputs_are_exact():
     w = _chain()
     o = oracle.verify_chain(w)
@@ -103,16 +112,21 @@ def test_close_test_exempts_from_that_step_on():
     g["out_tokens"][b, 1] = g["bonus"][b] = 3
     g["accept_rows"][b] = -1
     g["accept_rows"][b, :2] = [b * L, b * L + 1]
-    g["commit_cu"] = np.concatenate([[0], np.cumsum(g["num_out"])]).astype(np.int32)
-    n = int(g["commit_cu"][-1])
-    rows = np.concatenate([g["accept_rows"][i, :g["num_out"][i]] for i in range(w.batch)])
-    g["commit_src_slot"][:n] = w.row_slots[rows]
-    g["commit_dst_pos"][:n] = np.concatenate([w.seq_lens[i] + np.arange(g["num_out"][i]) for i in range(w.batch)])
+    _recommit(w, g)
     res = compare(w2, g, o2)
     assert res["test_flagged"] == 1 and res["differ"] == 1 and res["mismatch"] == 0
     # rejecting at step 0 contradicts a certain decision
     bad = copy.deepcopy(g)
     bad["accept_len"][b], bad["num_out"][b] = 0, 1
+    assert compare(w2, bad, o2, check=False)["mismatch"] >= 1
+    # ... even as a valid verification of its own (one correction token at row 0, consistent commit lists)
+    bad = copy.deepcopy(g)
+    bad["accept_len"][b], bad["num_out"][b] = 0, 1
+    bad["out_tokens"][b] = -1
+    bad["out_tokens"][b, 0] = bad["bonus"][b] = 3
+    bad["accept_rows"][b] = -1
+    bad["accept_rows"][b, 0] = b * L
+    _recommit(w, bad)
     assert compare(w2, bad, o2, check=False)["mismatch"] >= 1
     # a token that is not the draft at an accepted row is invalid
     bad = copy.deepcopy(g)
