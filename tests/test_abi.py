@@ -99,6 +99,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify_target_only_tree(fake, 1, 64, 2, 8, 64, fake, fake, null, null, fake,
                                             ctypes.c_float(1.0), ctypes.c_float(0.0), fake, fake, null, null,
                                             ctypes.byref(out2), ws, 1 << 30, null) == 2
+    for th_single, th_acc in ((1.0, float("inf")), (float("nan"), 1.0), (1.0, -0.5)):
+        assert lib.spec_verify_target_only_tree(fake, 1, 64, 2, 8, 64, fake, fake, null, null, fake,
+                                                ctypes.c_float(th_single), ctypes.c_float(th_acc), fake, fake, null,
+                                                null, ctypes.byref(out2), ws, 1 << 30, null) == 2
     # rejection: q missing, q stride misaligned
     assert lib.spec_verify_rejection_chain(fake, 1, 64, 2, 3, 64, fake, null, 64, fake, fake, fake, null, null,
                                            ctypes.byref(out2), ws, 1 << 30, null) == 1
